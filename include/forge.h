@@ -1,0 +1,171 @@
+/*
+ * forge.h -- C ABI of libforge.so: the weight-gradient GEMM dW = X^T dY with
+ * the optimizer step fused into its tiled epilogue, for NVIDIA GB300
+ * (compute capability 10.3, sm_103a).
+ *
+ * What the operations are (FORGE assessment PR, tessera#565, "docs(audit):
+ * FORGE assessment + residency-aware epilogue-fusion track"):
+ *   - The weight gradient of a linear layer is dW = X^T dY ("What's already
+ *     in tree and easy to miss": dRhs = matmul(lhs, dy, transposeA=true)).
+ *   - The optimizer step runs in the GEMM's tiled epilogue, so the gradient
+ *     never reaches device memory (opening paragraph).  Each output tile is
+ *     owned by one CTA and keeps the whole token dimension K (the full_k
+ *     legality condition of FORGE Prop. 1, same section), so there is no
+ *     split-K and no atomic accumulation; results are bitwise reproducible
+ *     ("Math verified, not asserted", P1).
+ *   - The fp32 accumulator feeds the optimizer state without truncation to
+ *     bf16 (P6; the "truncf" item of "What's already in tree").
+ *   - AdamW and SGD with momentum are the optimizers ("Claim hygiene on the
+ *     source").  AdamW follows torch.optim.AdamW: W <- W (1 - lr wd);
+ *     m <- b1 m + (1-b1) g; v <- b2 v + (1-b2) g^2;
+ *     W <- W - lr (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps).
+ *     SGD follows torch.optim.SGD (dampening 0, no Nesterov):
+ *     g' = g + wd W; buf <- mu buf + g'; W <- W - lr buf.
+ *   - Gradient clipping is not offered: exact global-norm clipping cannot be
+ *     fused ("Math verified, not asserted", P2).
+ *   - A routed (expert) weight whose expert received no tokens still takes
+ *     the step with g = 0, i.e. m and v decay by b1, b2 and W by its weight
+ *     decay (P5).
+ *
+ * Layouts (all row-major, element strides 1, no padding):
+ *   X  [K, N]   activations, token-major (K tokens, N = d_in)
+ *   dY [K, M]   output gradients, token-major (M = d_out)
+ *   W, m, v, buf, dW  [N, M]   ([E, N, M] for the grouped call)
+ *   dW[n][m] = sum_k X[k][n] * dY[k][m]  (times sX * sdY for e4m3 inputs)
+ * An nn.Linear weight [d_out, d_in] is the transpose of W; pass it as its
+ * [d_in, d_out] row-major view.
+ *
+ * Ownership and ordering: every pointer is caller-owned device memory.  The
+ * library allocates nothing per call and keeps no pointer after the call
+ * returns.  W, m, v, buf are updated in place.  Calls are asynchronous and
+ * ordered on `stream`; the return value reports only host-side validation
+ * and launch errors.  Errors detected on the device (a bounded wait that
+ * ran out) are recorded in a device status word read by
+ * forge_get_device_status().
+ *
+ * Caller preconditions (not checked):
+ *   - X and dY do not overlap W, m, v, buf or dW.
+ *   - dX = dY W^T has already consumed the old W (the in-place
+ *     "dX-before-update" hazard, "Math verified, not asserted", P1).
+ *   - W's whole gradient for this step is X^T dY: no tied or shared use
+ *     (the single-use guard of P1).
+ *
+ * Host-side checks run before any CUDA call, in this order: null pointers
+ * (X and dY may be NULL only when K == 0), sizes (M >= 1, N >= 1, K >= 0,
+ * E >= 1, step >= 1), dtypes, then the device (compute capability 10.3),
+ * then alignment (16-byte aligned bases of X, dY; 4-byte of W, m, v, dW;
+ * see FORGE_ERR_MISALIGNED).
+ */
+#ifndef FORGE_H
+#define FORGE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers (same underlying type). */
+typedef struct CUstream_st* forge_stream_t;
+
+typedef enum {
+    FORGE_OK = 0,
+    FORGE_ERR_INVALID_ARG = -1,       /* null pointer, bad size or hyperparameter */
+    FORGE_ERR_UNSUPPORTED_DTYPE = -2, /* dtype outside the supported set */
+    FORGE_ERR_UNSUPPORTED_DEVICE = -3,/* no device, or compute capability != 10.3 */
+    FORGE_ERR_MISALIGNED = -4,        /* a base pointer or row stride the kernels cannot address */
+    FORGE_ERR_CUDA = -5,              /* a CUDA runtime / driver call failed */
+    FORGE_ERR_TIMEOUT = -6            /* a device-side bounded wait ran out */
+} forge_status;
+
+typedef enum {
+    FORGE_BF16 = 0, /* bfloat16 */
+    FORGE_E4M3 = 1, /* OCP fp8 E4M3 ("fn": no infinities, max 448) */
+    FORGE_F32 = 2   /* IEEE binary32 */
+} forge_dtype;
+
+/*
+ * Fused dW = X^T dY and one AdamW step on W, m, v.
+ *   X, dY        device, [K, N] and [K, M] of in_dtype (FORGE_BF16 or
+ *                FORGE_E4M3).  K may be 0: the step then runs with g = 0.
+ *   W            device fp32 [N, M], updated in place.
+ *   m, v         device [N, M] of state_dtype (FORGE_F32 or FORGE_BF16),
+ *                updated in place.  With bf16 state, W is updated from the
+ *                unrounded fp32 m, v and then m, v are stored rounded to
+ *                nearest even.
+ *   lr, beta1, beta2, eps, wd   AdamW hyperparameters (0 < beta < 1,
+ *                lr >= 0, eps >= 0, wd >= 0).
+ *   step         1-based step count after incrementing (as torch's AdamW).
+ *   scales       device fp32 [2] = {sX, sdY} for FORGE_E4M3 inputs (the
+ *                gradient is sX * sdY * X^T dY); must be NULL for bf16.
+ * Row strides: N * elemsize(in_dtype) and M * elemsize(in_dtype) bytes.
+ */
+forge_status forge_wgrad_adamw(const void* X, const void* dY, float* W, void* m, void* v,
+                               int64_t M, int64_t N, int64_t K, forge_dtype in_dtype,
+                               forge_dtype state_dtype, float lr, float beta1, float beta2,
+                               float eps, float wd, int64_t step, const float* scales,
+                               forge_stream_t stream);
+
+/*
+ * Fused dW = X^T dY and one SGD-momentum step on W and the momentum buffer
+ * mom ([N, M] of state_dtype).  On the first step pass mom = 0 (then
+ * mom' = g + wd W, as torch's SGD).  Other arguments as forge_wgrad_adamw.
+ */
+forge_status forge_wgrad_sgdm(const void* X, const void* dY, float* W, void* mom, int64_t M,
+                              int64_t N, int64_t K, forge_dtype in_dtype, forge_dtype state_dtype,
+                              float lr, float momentum, float wd, const float* scales,
+                              forge_stream_t stream);
+
+/*
+ * dW = X^T dY alone, stored as fp32 [N, M] into dW (device).  This is the
+ * only call that writes a gradient to device memory; it exists to check the
+ * contraction by itself.
+ */
+forge_status forge_wgrad_only(const void* X, const void* dY, float* dW, int64_t M, int64_t N,
+                              int64_t K, forge_dtype in_dtype, const float* scales,
+                              forge_stream_t stream);
+
+/*
+ * Grouped (mixture-of-experts) form: E experts, each with its own W, m, v
+ * block [N, M] (stacked as [E, N, M]) and its own token rows.  X [T, N] and
+ * dY [T, M] hold the tokens packed by expert: expert e owns rows
+ * [offsets[e], offsets[e+1]) (offsets: device int32 [E+1], non-decreasing,
+ * offsets[0] >= 0, read on the device, so no host synchronisation).
+ * The gradient of expert e is X_e^T dY_e over its own rows only.  An expert
+ * with no rows still takes the AdamW step with g = 0 (P5).  `step` is the
+ * same for every expert.  T_total = offsets[E] is bounded by `T_max`
+ * (the number of rows of the X, dY allocations).  1 <= E <= 1024.
+ */
+forge_status forge_grouped_wgrad_adamw(const void* X, const void* dY, float* W, void* m, void* v,
+                                       const int32_t* offsets, int32_t E, int64_t T_max,
+                                       int64_t M, int64_t N, forge_dtype in_dtype,
+                                       forge_dtype state_dtype, float lr, float beta1, float beta2,
+                                       float eps, float wd, int64_t step, const float* scales,
+                                       forge_stream_t stream);
+
+/* Static description of a status code; never NULL. */
+const char* forge_status_string(forge_status status);
+
+/*
+ * Read and clear the device status word of the current device: FORGE_OK, or
+ * FORGE_ERR_TIMEOUT if a kernel's bounded wait ran out since the last read.
+ * Synchronises the current device.
+ */
+forge_status forge_get_device_status(void);
+
+/*
+ * Failure-detection self-test: launches one CTA that waits on a barrier no
+ * one arrives at, with a limit of timeout_us microseconds; the wait runs out,
+ * the kernel records FORGE_ERR_TIMEOUT in the device status word and
+ * returns normally (no trap, the context stays usable).
+ */
+forge_status forge_selftest_wait_timeout(uint32_t timeout_us, forge_stream_t stream);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int32_t forge_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FORGE_H */

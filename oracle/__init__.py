@@ -1,0 +1,276 @@
+"""fp64 CPU oracle for the fused weight-gradient GEMM + optimizer step.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline / reference legs of ``bench.py`` may import this package.
+The product path (``weight_grad_gemm_gb300``) never imports it and has no CPU
+fallback.
+
+The arithmetic lives in ``forge_oracle.c`` (plain C loops in double
+precision, compiled with ``-ffp-contract=off``); this module only builds that
+file with gcc, loads it with ctypes and marshals numpy arrays.  Array
+conventions:
+
+* bf16 tensors are passed as their raw 16-bit patterns (``np.uint16``),
+  e4m3 tensors as raw bytes (``np.uint8``), fp32 as ``np.float32``;
+  ``as_bits`` converts torch CPU tensors to those forms.
+* X is [K, N], dY is [K, M], all parameters and state are [N, M] row-major
+  (or [E, N, M] for the grouped routine); the gradient is dW = X^T dY.
+
+Sources: the FORGE assessment PR (tessera#565), "What's already in tree and
+easy to miss" (dRhs = matmul(lhs, dy, transposeA=true); K kept whole) and
+"Math verified, not asserted" (P1 partition independence, P5 zero-token
+decay, P6 no truncation); AdamW / SGD-momentum in PyTorch's formulation.
+
+Parity pins for every routine are in ``tests/test_oracle.py``; none is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+BF16, E4M3, F32 = 0, 1, 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "forge_oracle.c")
+_SO = os.path.join(_HERE, "_build", "libforge_oracle.so")
+_lib = None
+
+_GCC_FLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+              "-ffp-contract=off", "-fno-fast-math"]
+
+
+def build(force: bool = False) -> str:
+    """Compile forge_oracle.c into oracle/_build/libforge_oracle.so."""
+    os.makedirs(os.path.dirname(_SO), exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *_GCC_FLAGS, "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_SO)
+        P, I64, D, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double, ctypes.c_int
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_double.restype = D
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_double.restype = D
+        lib.oracle_double_to_bf16.argtypes = [D]
+        lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_decode.argtypes = [P, I, I64, P]
+        lib.oracle_round_bf16.argtypes = [P, I64, P]
+        lib.oracle_wgrad_rows.argtypes = [P, P, I, I64, I64, I64, I64, D, D, P, I64, P]
+        lib.oracle_wgrad_elem.argtypes = [P, P, I, I64, I64, I64, I64, D, D, I64, I64]
+        lib.oracle_wgrad_elem.restype = D
+        lib.oracle_adamw.argtypes = [I64, P, P, P, P, I, D, D, D, D, D, I64, P, P, P, P, P, P]
+        lib.oracle_sgdm.argtypes = [I64, P, P, P, I, D, D, D, P, P, P, P]
+        lib.oracle_wgrad_adamw_tiled.argtypes = [P, P, I, I64, I64, I64, D, D, P, P, P, I,
+                                                 D, D, D, D, D, I64, I64, I64, P, P, P]
+        lib.oracle_grouped_adamw.argtypes = [P, P, I, P, I64, I64, I64, D, D, P, P, P, I,
+                                             D, D, D, D, D, I64, P, I64, P, P, P, P, P, P, P]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def as_bits(t):
+    """torch CPU tensor or numpy array -> the raw numpy form the oracle takes."""
+    if isinstance(t, np.ndarray):
+        return np.ascontiguousarray(t)
+    import torch  # plain CPU use only
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).numpy()
+    if t.dtype == torch.float32:
+        return t.numpy()
+    if t.dtype in (torch.int32, torch.int64):
+        return t.numpy()
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _dtype_of(a: np.ndarray) -> int:
+    if a.dtype == np.uint16:
+        return BF16
+    if a.dtype == np.uint8:
+        return E4M3
+    if a.dtype == np.float32:
+        return F32
+    raise TypeError(f"unsupported array dtype {a.dtype}")
+
+
+def _state_dtype(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"state must be float32 or bf16 bits, got {a.dtype}")
+
+
+# ---- scalar helpers -------------------------------------------------------
+
+def bf16_to_double(h: int) -> float:
+    return _load().oracle_bf16_to_double(int(h))
+
+
+def e4m3_to_double(c: int) -> float:
+    return _load().oracle_e4m3_to_double(int(c))
+
+
+def double_to_bf16(x: float) -> int:
+    return int(_load().oracle_double_to_bf16(float(x)))
+
+
+def decode(bits: np.ndarray) -> np.ndarray:
+    """Raw bf16 / e4m3 / fp32 array -> float64, exactly."""
+    bits = np.ascontiguousarray(bits)
+    out = np.empty(bits.shape, np.float64)
+    _load().oracle_decode(_ptr(bits), _dtype_of(bits), bits.size, _ptr(out))
+    return out
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """float64 -> bf16 bit patterns, round to nearest, ties to even."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, np.uint16)
+    _load().oracle_round_bf16(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+# ---- the contraction ------------------------------------------------------
+
+def wgrad(X, dY, scales=(1.0, 1.0), rows=None, k_range=None) -> np.ndarray:
+    """g = sX * sdY * X^T dY in float64, [len(rows) or N, M].
+
+    X: [K, N] and dY: [K, M] raw bf16 (uint16) or e4m3 (uint8) arrays.
+    rows: optional list of output rows n; k_range: optional (k_begin, k_end)
+    restricting the contraction to those token rows.
+    """
+    X = as_bits(X)
+    dY = as_bits(dY)
+    dt = _dtype_of(X)
+    assert _dtype_of(dY) == dt and X.ndim == 2 and dY.ndim == 2 and X.shape[0] == dY.shape[0]
+    K, N = X.shape
+    M = dY.shape[1]
+    kb, ke = (0, K) if k_range is None else k_range
+    if rows is None:
+        r, nr = None, N
+    else:
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        nr = r.size
+    G = np.empty((nr, M), np.float64)
+    _load().oracle_wgrad_rows(_ptr(X), _ptr(dY), dt, M, N, kb, ke,
+                              float(scales[0]), float(scales[1]), _ptr(r), nr, _ptr(G))
+    return G
+
+
+def wgrad_elem(X, dY, n, m, scales=(1.0, 1.0), k_range=None) -> float:
+    X = as_bits(X)
+    dY = as_bits(dY)
+    K, N = X.shape
+    M = dY.shape[1]
+    kb, ke = (0, K) if k_range is None else k_range
+    return _load().oracle_wgrad_elem(_ptr(X), _ptr(dY), _dtype_of(X), M, N, kb, ke,
+                                     float(scales[0]), float(scales[1]), int(n), int(m))
+
+
+# ---- optimizer steps ------------------------------------------------------
+
+def adamw(G, W, m, v, lr, beta1, beta2, eps, wd, step) -> dict:
+    """One AdamW step on every element.  G float64, W float32, m/v float32
+    or bf16 bits (same type).  Returns W, m, v (stored types) and the
+    unrounded W_exact, m_exact, v_exact."""
+    G = np.ascontiguousarray(G, dtype=np.float64)
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    m = as_bits(m)
+    v = as_bits(v)
+    sd = _state_dtype(m)
+    assert _state_dtype(v) == sd and G.size == W.size == m.size == v.size
+    out = dict(W=np.empty_like(W), m=np.empty_like(m), v=np.empty_like(v),
+               W_exact=np.empty(W.shape, np.float64), m_exact=np.empty(W.shape, np.float64),
+               v_exact=np.empty(W.shape, np.float64))
+    _load().oracle_adamw(W.size, _ptr(G), _ptr(W), _ptr(m), _ptr(v), sd, float(lr),
+                         float(beta1), float(beta2), float(eps), float(wd), int(step),
+                         _ptr(out["W"]), _ptr(out["m"]), _ptr(out["v"]),
+                         _ptr(out["W_exact"]), _ptr(out["m_exact"]), _ptr(out["v_exact"]))
+    return out
+
+
+def sgdm(G, W, buf, lr, momentum, wd) -> dict:
+    """One SGD-momentum step.  Returns W, buf and W_exact, buf_exact."""
+    G = np.ascontiguousarray(G, dtype=np.float64)
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    buf = as_bits(buf)
+    sd = _state_dtype(buf)
+    assert G.size == W.size == buf.size
+    out = dict(W=np.empty_like(W), buf=np.empty_like(buf),
+               W_exact=np.empty(W.shape, np.float64), buf_exact=np.empty(W.shape, np.float64))
+    _load().oracle_sgdm(W.size, _ptr(G), _ptr(W), _ptr(buf), sd, float(lr), float(momentum),
+                        float(wd), _ptr(out["W"]), _ptr(out["buf"]), _ptr(out["W_exact"]),
+                        _ptr(out["buf_exact"]))
+    return out
+
+
+def wgrad_adamw_tiled(X, dY, W, m, v, lr, beta1, beta2, eps, wd, step,
+                      tile_n=0, tile_m=0, scales=(1.0, 1.0)) -> dict:
+    """dW = X^T dY + AdamW evaluated tile by tile (0 = whole extent)."""
+    X = as_bits(X)
+    dY = as_bits(dY)
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    m = as_bits(m)
+    v = as_bits(v)
+    K, N = X.shape
+    M = dY.shape[1]
+    out = dict(W=np.empty_like(W), m=np.empty_like(m), v=np.empty_like(v))
+    _load().oracle_wgrad_adamw_tiled(_ptr(X), _ptr(dY), _dtype_of(X), M, N, K,
+                                     float(scales[0]), float(scales[1]), _ptr(W), _ptr(m),
+                                     _ptr(v), _state_dtype(m), float(lr), float(beta1),
+                                     float(beta2), float(eps), float(wd), int(step),
+                                     int(tile_n), int(tile_m), _ptr(out["W"]), _ptr(out["m"]),
+                                     _ptr(out["v"]))
+    return out
+
+
+def grouped_adamw(X, dY, offsets, W, m, v, lr, beta1, beta2, eps, wd, step,
+                  rows=None, scales=(1.0, 1.0)) -> dict:
+    """Per-expert wgrad + AdamW.  X [T, N], dY [T, M] packed by expert,
+    offsets [E+1], W/m/v [E, N, M].  Returns [E, len(rows) or N, M] arrays."""
+    X = as_bits(X)
+    dY = as_bits(dY)
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    E = off.size - 1
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    m = as_bits(m)
+    v = as_bits(v)
+    N = X.shape[1]
+    M = dY.shape[1]
+    assert W.shape == (E, N, M)
+    if rows is None:
+        r, nr = None, N
+    else:
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        nr = r.size
+    shp = (E, nr, M)
+    out = dict(W=np.empty(shp, np.float32), m=np.empty(shp, m.dtype), v=np.empty(shp, v.dtype),
+               W_exact=np.empty(shp, np.float64), m_exact=np.empty(shp, np.float64),
+               v_exact=np.empty(shp, np.float64))
+    scratch = np.empty((nr, M), np.float64)
+    _load().oracle_grouped_adamw(_ptr(X), _ptr(dY), _dtype_of(X), _ptr(off), E, M, N,
+                                 float(scales[0]), float(scales[1]), _ptr(W), _ptr(m), _ptr(v),
+                                 _state_dtype(m), float(lr), float(beta1), float(beta2),
+                                 float(eps), float(wd), int(step), _ptr(r), nr, _ptr(scratch),
+                                 _ptr(out["W"]), _ptr(out["m"]), _ptr(out["v"]),
+                                 _ptr(out["W_exact"]), _ptr(out["m_exact"]), _ptr(out["v_exact"]))
+    return out

@@ -1,0 +1,381 @@
+"""Pins for the fp64 CPU oracle.
+
+Each check ties the oracle to something other than itself: brute-force
+integer arithmetic, a library routine on a special case (numpy matmul,
+torch CPU float64 AdamW / SGD, torch dtype casts), a closed form, or an
+invariant the FORGE assessment states (P1 partition independence, P5
+zero-token decay).  A plausible slip in the oracle -- a transposed operand,
+a dropped bias correction, a wrong sign, an index off by one expert --
+fails at least one of them.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return oracle.as_bits(t.to(torch.bfloat16))
+
+
+def rand_bf16(shape, seed, std=1.0):
+    return bf16_bits(wl.randn(shape, seed, std=std))
+
+
+# ---- decoders ---------------------------------------------------------------
+
+def test_e4m3_all_codes_match_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert nan.sum() == 2  # 0x7F and 0xFF
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert oracle.e4m3_to_double(0x7E) == 448.0
+    assert oracle.e4m3_to_double(0x01) == 2.0 ** -9
+
+
+def test_bf16_all_codes_match_torch():
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.decode(codes)
+    ref = torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_round_bf16_matches_torch_on_fp32_values():
+    # binary32 inputs: torch's float -> bfloat16 cast rounds to nearest even
+    # in one step, so it is an independent reference there.
+    x = torch.randn(200000, generator=torch.Generator().manual_seed(3)) * 7.0
+    x = torch.cat([x, torch.tensor([0.0, -0.0, 1e-40, -3e-39, 3.3e38, -3.39e38])])
+    ours = oracle.round_bf16(x.double().numpy())
+    ref = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_round_bf16_ties_to_even_and_nearest():
+    # exact midpoints between consecutive bf16 values round to the even one
+    for base_bits in (0x3F80, 0x3F81, 0x4049, 0xC123, 0x0001, 0x7F7E):
+        lo = oracle.bf16_to_double(base_bits)
+        hi = oracle.bf16_to_double(base_bits + 1)
+        mid = (lo + hi) / 2.0  # exact in binary64
+        want = base_bits if base_bits % 2 == 0 else base_bits + 1
+        assert oracle.double_to_bf16(mid) == want
+    # values that are not binary32-representable: check "nearest" exactly
+    rng = np.random.default_rng(11)
+    xs = rng.standard_normal(2000) * 10.0 ** rng.integers(-30, 30, 2000)
+    for x in xs:
+        b = oracle.double_to_bf16(x)
+        got = Fraction(oracle.bf16_to_double(b))
+        for nb in (b - 1, b + 1):
+            other = Fraction(oracle.bf16_to_double(nb))
+            assert abs(got - Fraction(x)) <= abs(other - Fraction(x))
+
+
+# ---- the contraction ---------------------------------------------------------
+
+def test_wgrad_bruteforce_4x4x8_integers():
+    # 4x4 output, K = 8: small integers are exact in bf16 and their dot
+    # products are exact integers, computed here with Python ints.
+    rng = np.random.default_rng(0)
+    Xi = rng.integers(-8, 9, size=(8, 4))
+    Di = rng.integers(-8, 9, size=(8, 4))
+    X = bf16_bits(torch.tensor(Xi, dtype=torch.float32))
+    D = bf16_bits(torch.tensor(Di, dtype=torch.float32))
+    G = oracle.wgrad(X, D)
+    for n in range(4):
+        for m in range(4):
+            want = sum(int(Xi[k, n]) * int(Di[k, m]) for k in range(8))
+            assert G[n, m] == want
+            assert oracle.wgrad_elem(X, D, n, m) == want
+
+
+def test_wgrad_orientation_is_x_transpose_dy():
+    # X = [[1,2],[3,4]], dY = I: dW[n][m] = X[m][n], i.e. dW = X^T.
+    X = bf16_bits(torch.tensor([[1.0, 2.0], [3.0, 4.0]]))
+    D = bf16_bits(torch.eye(2))
+    assert np.array_equal(oracle.wgrad(X, D), np.array([[1.0, 3.0], [2.0, 4.0]]))
+
+
+def test_wgrad_matches_numpy_fp64():
+    X = rand_bf16((200, 37), 1)
+    D = rand_bf16((200, 53), 2)
+    G = oracle.wgrad(X, D)
+    ref = oracle.decode(X).T @ oracle.decode(D)
+    assert np.max(np.abs(G - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+def test_wgrad_one_hot_rows_copy_dy_rows():
+    K, N, M = 24, 16, 40
+    perm = np.random.default_rng(5).permutation(K)[:N]
+    Xf = np.zeros((K, N), np.float32)
+    Xf[perm, np.arange(N)] = 1.0
+    X = bf16_bits(torch.from_numpy(Xf))
+    D = rand_bf16((K, M), 6)
+    G = oracle.wgrad(X, D)
+    assert np.array_equal(G, oracle.decode(D)[perm])
+
+
+def test_wgrad_rows_k_range_and_scales():
+    X = rand_bf16((64, 20), 7)
+    D = rand_bf16((64, 30), 8)
+    full = oracle.wgrad(X, D)
+    rows = [19, 0, 7]
+    part = oracle.wgrad(X, D, rows=rows)
+    assert np.array_equal(part, full[rows])
+    a = oracle.wgrad(X, D, k_range=(0, 40))
+    b = oracle.wgrad(X, D, k_range=(40, 64))
+    ref = oracle.decode(X).T @ oracle.decode(D)
+    assert np.max(np.abs(a + b - ref)) <= 1e-12 * np.max(np.abs(ref))
+    assert np.array_equal(oracle.wgrad(X, D, k_range=(5, 5)), np.zeros((20, 30)))
+    sc = oracle.wgrad(X, D, scales=(0.5, 0.25))
+    assert np.array_equal(sc, full * 0.125)
+
+
+def test_wgrad_e4m3_matches_numpy():
+    t = wl.with_outliers((96, 48), 9)
+    u = wl.with_outliers((96, 40), 10)
+    cx, sx = wl.quantize_e4m3(t)
+    cy, sy = wl.quantize_e4m3(u)
+    X, D = oracle.as_bits(cx), oracle.as_bits(cy)
+    G = oracle.wgrad(X, D, scales=(sx, sy))
+    ref = (cx.to(torch.float64).numpy().T @ cy.to(torch.float64).numpy()) * (sx * sy)
+    assert np.max(np.abs(G - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+# ---- AdamW -------------------------------------------------------------------
+
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.01)
+
+
+def test_adamw_first_step_closed_form_sign():
+    # t = 1, eps = 0: m1/bc1 = g and sqrt(v1/bc2) = |g|, so W1 = W0(1-lr wd) - lr sign(g)
+    rng = np.random.default_rng(1)
+    P = 5000
+    G = rng.standard_normal(P) * 10.0 ** rng.integers(-6, 3, P)
+    W = (rng.standard_normal(P) * 0.02).astype(np.float32)
+    z = np.zeros(P, np.float32)
+    lr, wd = 1e-3, 0.01
+    out = oracle.adamw(G, W, z, z, lr=lr, beta1=0.9, beta2=0.999, eps=0.0, wd=wd, step=1)
+    want = W.astype(np.float64) * (1 - lr * wd) - lr * np.sign(G)
+    assert np.max(np.abs(out["W_exact"] - want)) <= 1e-15
+    assert np.array_equal(out["W"], want.astype(np.float32)) or \
+        np.max(np.abs(out["W"].astype(np.float64) - want)) <= 1e-9
+
+
+def test_adamw_zero_gradient_is_exact_decay():
+    rng = np.random.default_rng(2)
+    P = 4096
+    W = (rng.standard_normal(P) * 0.02).astype(np.float32)
+    m = (rng.standard_normal(P) * 1e-3).astype(np.float32)
+    v = (rng.random(P) * 1e-6).astype(np.float32)
+    out = oracle.adamw(np.zeros(P), W, m, v, step=7, **HP)
+    assert np.array_equal(out["m_exact"], 0.9 * m.astype(np.float64))
+    assert np.array_equal(out["v_exact"], 0.999 * v.astype(np.float64))
+    assert np.array_equal(out["m"], (0.9 * m.astype(np.float64)).astype(np.float32))
+    assert np.array_equal(out["v"], (0.999 * v.astype(np.float64)).astype(np.float32))
+
+
+@pytest.mark.parametrize("step", [1, 4, 50])
+def test_adamw_matches_torch_float64(step):
+    rng = np.random.default_rng(step)
+    P = 3000
+    G = rng.standard_normal(P) * 1e-2
+    W = (rng.standard_normal(P) * 0.02).astype(np.float32)
+    if step == 1:
+        m = np.zeros(P, np.float32)
+        v = np.zeros(P, np.float32)
+    else:
+        m = (rng.standard_normal(P) * 1e-3).astype(np.float32)
+        v = (rng.random(P) * 1e-4).astype(np.float32)
+    hp = dict(lr=3e-3, beta1=0.85, beta2=0.995, eps=1e-6, wd=0.1)
+    out = oracle.adamw(G, W, m, v, step=step, **hp)
+
+    p = torch.nn.Parameter(torch.from_numpy(W.astype(np.float64)))
+    opt = torch.optim.AdamW([p], lr=hp["lr"], betas=(hp["beta1"], hp["beta2"]), eps=hp["eps"],
+                            weight_decay=hp["wd"], foreach=False)
+    opt.state[p] = {"step": torch.tensor(float(step - 1)),
+                    "exp_avg": torch.from_numpy(m.astype(np.float64)),
+                    "exp_avg_sq": torch.from_numpy(v.astype(np.float64))}
+    p.grad = torch.from_numpy(G)
+    opt.step()
+    tw = p.detach().numpy()
+    assert np.max(np.abs(out["W_exact"] - tw)) <= 1e-15 * max(1.0, np.max(np.abs(tw)))
+    tm = opt.state[p]["exp_avg"].numpy()
+    tv = opt.state[p]["exp_avg_sq"].numpy()
+    assert np.max(np.abs(out["m_exact"] - tm)) <= 1e-15 * np.max(np.abs(tm))
+    assert np.max(np.abs(out["v_exact"] - tv)) <= 1e-15 * np.max(np.abs(tv))
+
+
+def test_adamw_bf16_state_is_rne_of_exact():
+    rng = np.random.default_rng(4)
+    P = 2048
+    G = rng.standard_normal(P) * 1e-2
+    W = (rng.standard_normal(P) * 0.02).astype(np.float32)
+    m = oracle.round_bf16(rng.standard_normal(P) * 1e-3)
+    v = oracle.round_bf16(rng.random(P) * 1e-4)
+    out = oracle.adamw(G, W, m, v, step=3, **HP)
+    assert out["m"].dtype == np.uint16
+    assert np.array_equal(out["m"], oracle.round_bf16(out["m_exact"]))
+    assert np.array_equal(out["v"], oracle.round_bf16(out["v_exact"]))
+    # the bf16 state is decoded exactly before use
+    f32 = oracle.adamw(G, W, oracle.decode(m).astype(np.float32),
+                       oracle.decode(v).astype(np.float32), step=3, **HP)
+    assert np.array_equal(f32["W_exact"], out["W_exact"])
+
+
+# ---- SGD momentum -------------------------------------------------------------
+
+def test_sgdm_constant_gradient_closed_form():
+    rng = np.random.default_rng(6)
+    P = 1000
+    g = rng.standard_normal(P)
+    W = np.zeros(P, np.float32)
+    buf = np.zeros(P, np.float32)
+    mu = 0.9
+    for t in range(1, 9):
+        out = oracle.sgdm(g, W, buf, lr=0.0, momentum=mu, wd=0.0)
+        want = g * (1 - mu ** t) / (1 - mu)
+        assert np.max(np.abs(out["buf_exact"] - want)) <= 1e-6 * np.max(np.abs(want))
+        buf = out["buf"]
+
+
+def test_sgdm_matches_torch_float64():
+    rng = np.random.default_rng(7)
+    P = 3000
+    G = rng.standard_normal(P) * 1e-2
+    W = (rng.standard_normal(P) * 0.02).astype(np.float32)
+    buf = (rng.standard_normal(P) * 1e-3).astype(np.float32)
+    out = oracle.sgdm(G, W, buf, lr=1e-2, momentum=0.9, wd=0.05)
+    p = torch.nn.Parameter(torch.from_numpy(W.astype(np.float64)))
+    opt = torch.optim.SGD([p], lr=1e-2, momentum=0.9, weight_decay=0.05, foreach=False)
+    opt.state[p] = {"momentum_buffer": torch.from_numpy(buf.astype(np.float64))}
+    p.grad = torch.from_numpy(G)
+    opt.step()
+    assert np.max(np.abs(out["W_exact"] - p.detach().numpy())) <= 1e-16
+    tb = opt.state[p]["momentum_buffer"].numpy()
+    assert np.max(np.abs(out["buf_exact"] - tb)) <= 1e-15 * np.max(np.abs(tb))
+    # first step: buf = 0 gives buf' = g + wd W, as torch's clone on step 1
+    z = np.zeros(P, np.float32)
+    first = oracle.sgdm(G, W, z, lr=1e-2, momentum=0.9, wd=0.05)
+    assert np.array_equal(first["buf_exact"], G + 0.05 * W.astype(np.float64))
+
+
+# ---- P1: per-tile exactness does not depend on the partition ------------------
+
+def test_tiled_fused_result_independent_of_tile_size():
+    K, N, M = 40, 70, 45
+    X = rand_bf16((K, N), 21, std=0.1)
+    D = rand_bf16((K, M), 22, std=0.1)
+    rng = np.random.default_rng(23)
+    W = (rng.standard_normal((N, M)) * 0.02).astype(np.float32)
+    m = (rng.standard_normal((N, M)) * 1e-3).astype(np.float32)
+    v = (rng.random((N, M)) * 1e-4).astype(np.float32)
+    results = [oracle.wgrad_adamw_tiled(X, D, W, m, v, step=2, tile_n=t, tile_m=t, **HP)
+               for t in (1, 3, 16, 64, 0)]
+    results.append(oracle.wgrad_adamw_tiled(X, D, W, m, v, step=2, tile_n=5, tile_m=64, **HP))
+    for r in results[1:]:
+        for k in ("W", "m", "v"):
+            assert np.array_equal(r[k], results[0][k])
+    # and equal to the unfused whole-tensor composition
+    G = oracle.wgrad(X, D)
+    un = oracle.adamw(G, W, m, v, step=2, **HP)
+    for k in ("W", "m", "v"):
+        assert np.array_equal(un[k], results[0][k])
+
+
+# ---- grouped ------------------------------------------------------------------
+
+def _grouped_case(counts, seed, N=24, M=20, state_bf16=False):
+    T = int(sum(counts))
+    E = len(counts)
+    X = rand_bf16((max(T, 1), N), seed, std=0.1)[:T]
+    D = rand_bf16((max(T, 1), M), seed + 1, std=0.1)[:T]
+    rng = np.random.default_rng(seed)
+    W = (rng.standard_normal((E, N, M)) * 0.02).astype(np.float32)
+    m = (rng.standard_normal((E, N, M)) * 1e-3).astype(np.float32)
+    v = (rng.random((E, N, M)) * 1e-4).astype(np.float32)
+    if state_bf16:
+        m, v = oracle.round_bf16(m), oracle.round_bf16(v)
+    return X, D, wl.offsets_from_counts(counts), W, m, v
+
+
+def test_grouped_single_expert_equals_dense():
+    X, D, off, W, m, v = _grouped_case([50], 30)
+    g = oracle.grouped_adamw(X, D, off, W, m, v, step=3, **HP)
+    dense = oracle.adamw(oracle.wgrad(X, D), W[0], m[0], v[0], step=3, **HP)
+    for k in ("W", "m", "v"):
+        assert np.array_equal(g[k][0], dense[k])
+
+
+def test_grouped_zero_token_expert_is_pure_decay():
+    X, D, off, W, m, v = _grouped_case([13, 0, 29, 0], 31)
+    g = oracle.grouped_adamw(X, D, off, W, m, v, step=5, **HP)
+    for e in (1, 3):
+        dec = oracle.adamw(np.zeros(W[e].size), W[e], m[e], v[e], step=5, **HP)
+        for k in ("W", "m", "v"):
+            assert np.array_equal(g[k][e], dec[k].reshape(W[e].shape))
+        assert np.array_equal(g["m_exact"][e], 0.9 * m[e].astype(np.float64))
+    for e in (0, 2):
+        Xe = X[off[e]:off[e + 1]]
+        De = D[off[e]:off[e + 1]]
+        ref = oracle.adamw(oracle.wgrad(Xe, De), W[e], m[e], v[e], step=5, **HP)
+        for k in ("W", "m", "v"):
+            assert np.array_equal(g[k][e], ref[k])
+
+
+@pytest.mark.parametrize("state_bf16", [False, True])
+def test_grouped_invariant_under_segment_permutation(state_bf16):
+    counts = [17, 5, 0, 30, 9]
+    X, D, off, W, m, v = _grouped_case(counts, 32, state_bf16=state_bf16)
+    base = oracle.grouped_adamw(X, D, off, W, m, v, step=2, **HP)
+    order = [3, 0, 4, 2, 1]  # new packing order of the expert segments
+    segs_x = [X[off[e]:off[e + 1]] for e in range(len(counts))]
+    segs_d = [D[off[e]:off[e + 1]] for e in range(len(counts))]
+    Xp = np.concatenate([segs_x[e] for e in order])
+    Dp = np.concatenate([segs_d[e] for e in order])
+    start = {}
+    pos = 0
+    for e in order:
+        start[e] = pos
+        pos += counts[e]
+    # the oracle takes monotone offsets, so compute each expert from its moved rows
+    for e in range(len(counts)):
+        sub_off = np.array([start[e], start[e] + counts[e]])
+        one = oracle.grouped_adamw(Xp, Dp, sub_off, W[e:e + 1], m[e:e + 1], v[e:e + 1],
+                                   step=2, **HP)
+        for k in ("W", "m", "v"):
+            assert np.array_equal(one[k][0], base[k][e])
+
+
+def test_grouped_row_subset_matches_full():
+    X, D, off, W, m, v = _grouped_case([11, 0, 7], 33)
+    full = oracle.grouped_adamw(X, D, off, W, m, v, step=4, **HP)
+    rows = [23, 2, 9]
+    part = oracle.grouped_adamw(X, D, off, W, m, v, step=4, rows=rows, **HP)
+    for k in ("W", "m", "v", "W_exact"):
+        assert np.array_equal(part[k], full[k][:, rows])
+
+
+# ---- cross-platform regression (fixture written by tests/golden/make_golden.py) ----
+
+def test_oracle_regression_fixture():
+    import json
+    import os
+    import sys
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    sys.path.insert(0, here)
+    try:
+        import make_golden
+    finally:
+        sys.path.remove(here)
+    with open(os.path.join(here, "oracle_regression.json")) as f:
+        want = json.load(f)["data"]
+    assert make_golden.compute() == want
