@@ -61,6 +61,12 @@
 
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define FORGE_API __attribute__((visibility("default")))
+#else
+#define FORGE_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -100,7 +106,7 @@ typedef enum {
  *                gradient is sX * sdY * X^T dY); must be NULL for bf16.
  * Row strides: N * elemsize(in_dtype) and M * elemsize(in_dtype) bytes.
  */
-forge_status forge_wgrad_adamw(const void* X, const void* dY, float* W, void* m, void* v,
+FORGE_API forge_status forge_wgrad_adamw(const void* X, const void* dY, float* W, void* m, void* v,
                                int64_t M, int64_t N, int64_t K, forge_dtype in_dtype,
                                forge_dtype state_dtype, float lr, float beta1, float beta2,
                                float eps, float wd, int64_t step, const float* scales,
@@ -111,7 +117,7 @@ forge_status forge_wgrad_adamw(const void* X, const void* dY, float* W, void* m,
  * mom ([N, M] of state_dtype).  On the first step pass mom = 0 (then
  * mom' = g + wd W, as torch's SGD).  Other arguments as forge_wgrad_adamw.
  */
-forge_status forge_wgrad_sgdm(const void* X, const void* dY, float* W, void* mom, int64_t M,
+FORGE_API forge_status forge_wgrad_sgdm(const void* X, const void* dY, float* W, void* mom, int64_t M,
                               int64_t N, int64_t K, forge_dtype in_dtype, forge_dtype state_dtype,
                               float lr, float momentum, float wd, const float* scales,
                               forge_stream_t stream);
@@ -121,7 +127,7 @@ forge_status forge_wgrad_sgdm(const void* X, const void* dY, float* W, void* mom
  * only call that writes a gradient to device memory; it exists to check the
  * contraction by itself.
  */
-forge_status forge_wgrad_only(const void* X, const void* dY, float* dW, int64_t M, int64_t N,
+FORGE_API forge_status forge_wgrad_only(const void* X, const void* dY, float* dW, int64_t M, int64_t N,
                               int64_t K, forge_dtype in_dtype, const float* scales,
                               forge_stream_t stream);
 
@@ -136,7 +142,7 @@ forge_status forge_wgrad_only(const void* X, const void* dY, float* dW, int64_t 
  * same for every expert.  T_total = offsets[E] is bounded by `T_max`
  * (the number of rows of the X, dY allocations).  1 <= E <= 1024.
  */
-forge_status forge_grouped_wgrad_adamw(const void* X, const void* dY, float* W, void* m, void* v,
+FORGE_API forge_status forge_grouped_wgrad_adamw(const void* X, const void* dY, float* W, void* m, void* v,
                                        const int32_t* offsets, int32_t E, int64_t T_max,
                                        int64_t M, int64_t N, forge_dtype in_dtype,
                                        forge_dtype state_dtype, float lr, float beta1, float beta2,
@@ -144,14 +150,14 @@ forge_status forge_grouped_wgrad_adamw(const void* X, const void* dY, float* W, 
                                        forge_stream_t stream);
 
 /* Static description of a status code; never NULL. */
-const char* forge_status_string(forge_status status);
+FORGE_API const char* forge_status_string(forge_status status);
 
 /*
  * Read and clear the device status word of the current device: FORGE_OK, or
  * FORGE_ERR_TIMEOUT if a kernel's bounded wait ran out since the last read.
  * Synchronises the current device.
  */
-forge_status forge_get_device_status(void);
+FORGE_API forge_status forge_get_device_status(void);
 
 /*
  * Failure-detection self-test: launches one CTA that waits on a barrier no
@@ -159,10 +165,10 @@ forge_status forge_get_device_status(void);
  * the kernel records FORGE_ERR_TIMEOUT in the device status word and
  * returns normally (no trap, the context stays usable).
  */
-forge_status forge_selftest_wait_timeout(uint32_t timeout_us, forge_stream_t stream);
+FORGE_API forge_status forge_selftest_wait_timeout(uint32_t timeout_us, forge_stream_t stream);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
-int32_t forge_version(void);
+FORGE_API int32_t forge_version(void);
 
 #ifdef __cplusplus
 }

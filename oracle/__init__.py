@@ -2,7 +2,7 @@
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
 the CPU-baseline / reference legs of ``bench.py`` may import this package.
-The product path (``weight_grad_gemm_gb300``) never imports it and has no CPU
+The product path (the CUDA library and its binding) never imports it and has no CPU
 fallback.
 
 The arithmetic lives in ``forge_oracle.c`` (plain C loops in double

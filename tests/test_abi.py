@@ -1,0 +1,124 @@
+"""C-ABI contract tests that need no GPU.
+
+The library must load on a machine without a GPU, export every function
+that include/forge.h declares, and reject invalid arguments with the
+documented status codes before making any CUDA call (the pages' fail-closed
+pattern: a GPU evidence command exits red on a missing or wrong device).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import weight_grad_gemm_gb300 as fg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "forge.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(fg.LIB_PATH):
+        from weight_grad_gemm_gb300 import build
+        build.build()
+    return fg.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"FORGE_API\s+[\w\s\*]+?\b(forge_\w+)\s*\(", text)
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert set(names) == set(fg.EXPORTS)
+    for n in ("forge_wgrad_adamw", "forge_wgrad_sgdm", "forge_wgrad_only",
+              "forge_grouped_wgrad_adamw", "forge_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert fg.forge_version() == 100
+
+
+def test_status_strings(L):
+    for code in range(-6, 1):
+        s = fg.forge_status_string(code)
+        assert isinstance(s, str) and s and s != "unknown status"
+    assert fg.forge_status_string(-99) == "unknown status"
+
+
+# A fake, never-dereferenced device address: every call below fails its host
+# checks before any pointer is used.
+FAKE = ctypes.c_void_p(0x10000)
+HP = (1e-3, 0.9, 0.999, 1e-8, 0.01)
+
+
+def adamw(L, X=FAKE, dY=FAKE, W=FAKE, m=FAKE, v=FAKE, M=64, N=64, K=64, it=fg.FORGE_BF16,
+          st=fg.FORGE_F32, hp=HP, step=1, scales=None):
+    return L.forge_wgrad_adamw(X, dY, W, m, v, M, N, K, it, st, *hp, step, scales, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(W=None), fg.FORGE_ERR_INVALID_ARG),
+    (dict(m=None), fg.FORGE_ERR_INVALID_ARG),
+    (dict(v=None), fg.FORGE_ERR_INVALID_ARG),
+    (dict(X=None), fg.FORGE_ERR_INVALID_ARG),
+    (dict(dY=None), fg.FORGE_ERR_INVALID_ARG),
+    (dict(M=0), fg.FORGE_ERR_INVALID_ARG),
+    (dict(N=-3), fg.FORGE_ERR_INVALID_ARG),
+    (dict(K=-1), fg.FORGE_ERR_INVALID_ARG),
+    (dict(M=1 << 31), fg.FORGE_ERR_INVALID_ARG),
+    (dict(step=0), fg.FORGE_ERR_INVALID_ARG),
+    (dict(it=fg.FORGE_F32), fg.FORGE_ERR_UNSUPPORTED_DTYPE),
+    (dict(it=7), fg.FORGE_ERR_UNSUPPORTED_DTYPE),
+    (dict(st=fg.FORGE_E4M3), fg.FORGE_ERR_UNSUPPORTED_DTYPE),
+    (dict(it=fg.FORGE_E4M3), fg.FORGE_ERR_INVALID_ARG),           # e4m3 needs scales
+    (dict(scales=FAKE), fg.FORGE_ERR_INVALID_ARG),               # bf16 takes no scales
+    (dict(hp=(1e-3, 1.0, 0.999, 1e-8, 0.01)), fg.FORGE_ERR_INVALID_ARG),
+    (dict(hp=(1e-3, 0.9, -0.1, 1e-8, 0.01)), fg.FORGE_ERR_INVALID_ARG),
+    (dict(hp=(float("nan"), 0.9, 0.999, 1e-8, 0.01)), fg.FORGE_ERR_INVALID_ARG),
+    (dict(hp=(1e-3, 0.9, 0.999, -1.0, 0.01)), fg.FORGE_ERR_INVALID_ARG),
+    (dict(hp=(1e-3, 0.9, 0.999, 1e-8, float("inf"))), fg.FORGE_ERR_INVALID_ARG),
+])
+def test_adamw_rejects_invalid_arguments(L, kw, code):
+    assert adamw(L, **kw) == code
+
+
+def test_sgdm_and_wgrad_only_reject_invalid_arguments(L):
+    assert L.forge_wgrad_sgdm(FAKE, FAKE, None, FAKE, 8, 8, 8, 0, 2, 1e-2, 0.9, 0.0, None,
+                              None) == fg.FORGE_ERR_INVALID_ARG
+    assert L.forge_wgrad_sgdm(FAKE, FAKE, FAKE, FAKE, 8, 8, 8, 0, 2, 1e-2, -0.9, 0.0, None,
+                              None) == fg.FORGE_ERR_INVALID_ARG
+    assert L.forge_wgrad_sgdm(FAKE, FAKE, FAKE, FAKE, 8, 8, 8, 0, 1, 1e-2, 0.9, 0.0, None,
+                              None) == fg.FORGE_ERR_UNSUPPORTED_DTYPE
+    assert L.forge_wgrad_only(FAKE, FAKE, None, 8, 8, 8, 0, None, None) == fg.FORGE_ERR_INVALID_ARG
+    assert L.forge_wgrad_only(FAKE, FAKE, FAKE, 8, 0, 8, 0, None, None) == fg.FORGE_ERR_INVALID_ARG
+    assert L.forge_wgrad_only(FAKE, FAKE, FAKE, 8, 8, 8, 3, None, None) == \
+        fg.FORGE_ERR_UNSUPPORTED_DTYPE
+
+
+def test_grouped_rejects_invalid_arguments(L):
+    def g(offs=FAKE, E=4, T=64, step=1):
+        return L.forge_grouped_wgrad_adamw(FAKE, FAKE, FAKE, FAKE, FAKE, offs, E, T, 64, 64, 0, 2,
+                                           *HP, step, None, None)
+    assert g(offs=None) == fg.FORGE_ERR_INVALID_ARG
+    assert g(E=0) == fg.FORGE_ERR_INVALID_ARG
+    assert g(E=1025) == fg.FORGE_ERR_INVALID_ARG
+    assert g(T=-1) == fg.FORGE_ERR_INVALID_ARG
+    assert g(step=0) == fg.FORGE_ERR_INVALID_ARG
+
+
+def test_selftest_rejects_bad_limit(L):
+    assert L.forge_selftest_wait_timeout(0, None) == fg.FORGE_ERR_INVALID_ARG
+
+
+def test_valid_call_without_gpu_fails_closed(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; the fake pointers must not reach a kernel")
+    assert adamw(L) == fg.FORGE_ERR_UNSUPPORTED_DEVICE
+    assert fg.forge_get_device_status() == fg.FORGE_ERR_UNSUPPORTED_DEVICE

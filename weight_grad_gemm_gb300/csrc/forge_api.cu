@@ -1,0 +1,403 @@
+// forge_api.cu -- the C ABI of libforge.so: argument validation, device
+// checks, TMA descriptor encoding, tile-grid sizing and kernel dispatch.
+//
+// Every check on the arguments runs before the first CUDA call, so invalid
+// calls fail with a status code even on a machine without a GPU.  The
+// library keeps no per-call allocation: the only device memory it owns is
+// the status word below, which exists once per device for the life of the
+// process.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "forge.h"
+#include "forge_launch.cuh"
+
+namespace {
+
+using namespace forge;
+
+constexpr int kMaxDevices = 64;
+
+// Device status word: 0, or the first device-side error since the last read.
+__device__ int g_forge_status = 0;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int sms = 0;
+    int* status = nullptr;  // device address of g_forge_status on this device
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int64_t wait_timeout_ns()
+{
+    static const int64_t v = [] {
+        const char* s = std::getenv("FORGE_WAIT_TIMEOUT_MS");
+        long long ms = s ? std::atoll(s) : 10000;
+        if (ms <= 0) ms = 10000;
+        return static_cast<int64_t>(ms) * 1000000;
+    }();
+    return v;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool finite_nonneg(float x) { return std::isfinite(x) && x >= 0.0f; }
+
+int elem_size(forge_dtype t) { return t == FORGE_BF16 ? 2 : (t == FORGE_E4M3 ? 1 : 4); }
+
+// Resolves the current device and caches its properties.  The first call on
+// a device also resolves the address of the status word there.
+forge_status current_device(DeviceInfo** out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return FORGE_ERR_UNSUPPORTED_DEVICE;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return FORGE_ERR_UNSUPPORTED_DEVICE;
+        }
+        d.supported = (major == 10 && minor == 3);
+        d.sms = sms;
+        if (d.supported) {
+            void* addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_forge_status) != cudaSuccess) {
+                cudaGetLastError();
+                return FORGE_ERR_CUDA;
+            }
+            d.status = static_cast<int*>(addr);
+        }
+        d.ready = true;
+    }
+    if (!d.supported) return FORGE_ERR_UNSUPPORTED_DEVICE;
+    *out = &d;
+    return FORGE_OK;
+}
+
+// 2-D token-major operand [rows, inner] -> TMA map with 128-byte swizzled
+// boxes of (128 bytes of the inner dimension) x (k rows per stage).
+forge_status encode_operand(CUtensorMap* map, const void* base, forge_dtype dt, int64_t inner,
+                            int64_t rows)
+{
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    });
+    if (!g_encode) return FORGE_ERR_CUDA;
+    const int es = elem_size(dt);
+    const cuuint32_t box_inner = 128 / es;
+    const cuuint32_t box_rows = dt == FORGE_BF16 ? InTraits<IN_BF16>::BK : InTraits<IN_E4M3>::BK;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * es};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType t =
+        dt == FORGE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = g_encode(map, t, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FORGE_OK : FORGE_ERR_CUDA;
+}
+
+// Failure-detection self-test: wait on a barrier no one arrives at.
+__global__ void forge_wait_selftest_kernel(int64_t timeout_ns, int* status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        abort_flag = 0;
+        ptx::fence_mbarrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        Params p{};
+        p.timeout_ns = timeout_ns;
+        p.status = status;
+        (void)wait_bounded(&bar, 0, &abort_flag, p);
+    }
+}
+
+forge_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FORGE_OK : FORGE_ERR_CUDA; }
+
+template <int IT>
+cudaError_t dispatch_op(int op, int st, bool grouped, const CUtensorMap& a, const CUtensorMap& b,
+                        const Params& p, int grid, cudaStream_t s)
+{
+    if (grouped) {
+        return st == ST_F32 ? launch_wgrad<IT, OP_ADAMW, ST_F32, true>(a, b, p, grid, s)
+                            : launch_wgrad<IT, OP_ADAMW, ST_BF16, true>(a, b, p, grid, s);
+    }
+    switch (op) {
+    case OP_ADAMW:
+        return st == ST_F32 ? launch_wgrad<IT, OP_ADAMW, ST_F32, false>(a, b, p, grid, s)
+                            : launch_wgrad<IT, OP_ADAMW, ST_BF16, false>(a, b, p, grid, s);
+    case OP_SGDM:
+        return st == ST_F32 ? launch_wgrad<IT, OP_SGDM, ST_F32, false>(a, b, p, grid, s)
+                            : launch_wgrad<IT, OP_SGDM, ST_BF16, false>(a, b, p, grid, s);
+    default:
+        return launch_wgrad<IT, OP_DW, ST_F32, false>(a, b, p, grid, s);
+    }
+}
+
+// Shared tail of every entry point, after the argument checks.
+//   rows: K (dense) or T_max (grouped) -- the rows of X and dY.
+forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dtype, int op,
+                 forge_dtype state_dtype, bool grouped, Params p, cudaStream_t stream)
+{
+    DeviceInfo* dev = nullptr;
+    forge_status st = current_device(&dev);
+    if (st != FORGE_OK) return st;
+
+    const int es = elem_size(in_dtype);
+    if (rows > 0) {
+        // TMA: 16-byte aligned bases and row strides
+        if (!aligned(X, 16) || !aligned(dY, 16) || (p.N * es) % 16 != 0 || (p.M * es) % 16 != 0)
+            return FORGE_ERR_MISALIGNED;
+    }
+    const uintptr_t sa = state_dtype == FORGE_BF16 ? 2 : 4;
+    if (!aligned(p.W, 4) || (p.s1 && !aligned(p.s1, sa)) || (p.s2 && !aligned(p.s2, sa)) ||
+        (p.dW && !aligned(p.dW, 4)))
+        return FORGE_ERR_MISALIGNED;
+
+    CUtensorMap tmA, tmB;
+    std::memset(&tmA, 0, sizeof tmA);
+    std::memset(&tmB, 0, sizeof tmB);
+    p.has_maps = rows > 0 ? 1 : 0;
+    if (rows > 0) {
+        if ((st = encode_operand(&tmA, dY, in_dtype, p.M, rows)) != FORGE_OK) return st;
+        if ((st = encode_operand(&tmB, X, in_dtype, p.N, rows)) != FORGE_OK) return st;
+    }
+    const int64_t tiles_m = (p.M + BM - 1) / BM;
+    const int64_t tiles_n = (p.N + BN - 1) / BN;
+    const int64_t total = tiles_m * tiles_n * p.E;
+    if (total <= 0 || total > INT32_MAX) return FORGE_ERR_INVALID_ARG;
+    p.tiles_m = static_cast<int32_t>(tiles_m);
+    p.tiles_n = static_cast<int32_t>(tiles_n);
+    p.timeout_ns = wait_timeout_ns();
+    p.status = dev->status;
+    const int grid = static_cast<int>(total < dev->sms ? total : dev->sms);
+
+    const int ist = state_dtype == FORGE_BF16 ? ST_BF16 : ST_F32;
+    cudaError_t e = in_dtype == FORGE_BF16
+                        ? dispatch_op<IN_BF16>(op, ist, grouped, tmA, tmB, p, grid, stream)
+                        : dispatch_op<IN_E4M3>(op, ist, grouped, tmA, tmB, p, grid, stream);
+    return from_cuda(e);
+}
+
+forge_status check_sizes(int64_t M, int64_t N, int64_t K)
+{
+    if (M < 1 || N < 1 || K < 0) return FORGE_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FORGE_ERR_INVALID_ARG;
+    return FORGE_OK;
+}
+
+forge_status check_inputs(const void* X, const void* dY, int64_t K, forge_dtype in_dtype,
+                          const float* scales)
+{
+    if (K > 0 && (!X || !dY)) return FORGE_ERR_INVALID_ARG;
+    if (in_dtype != FORGE_BF16 && in_dtype != FORGE_E4M3) return FORGE_ERR_UNSUPPORTED_DTYPE;
+    if (in_dtype == FORGE_E4M3 && !scales) return FORGE_ERR_INVALID_ARG;
+    if (in_dtype == FORGE_BF16 && scales) return FORGE_ERR_INVALID_ARG;
+    return FORGE_OK;
+}
+
+forge_status check_adam(float lr, float beta1, float beta2, float eps, float wd, int64_t step)
+{
+    if (step < 1) return FORGE_ERR_INVALID_ARG;
+    if (!finite_nonneg(lr) || !finite_nonneg(eps) || !finite_nonneg(wd)) return FORGE_ERR_INVALID_ARG;
+    if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
+        return FORGE_ERR_INVALID_ARG;
+    return FORGE_OK;
+}
+
+void fill_adam(Params& p, float lr, float beta1, float beta2, float eps, float wd, int64_t step)
+{
+    // Bias corrections in double, as torch computes them on the host.
+    const double bc1 = 1.0 - std::pow(static_cast<double>(beta1), static_cast<double>(step));
+    const double bc2 = 1.0 - std::pow(static_cast<double>(beta2), static_cast<double>(step));
+    p.decay = static_cast<float>(1.0 - static_cast<double>(lr) * wd);
+    p.b1 = beta1;
+    p.omb1 = static_cast<float>(1.0 - static_cast<double>(beta1));
+    p.b2 = beta2;
+    p.omb2 = static_cast<float>(1.0 - static_cast<double>(beta2));
+    p.step_size = static_cast<float>(lr / bc1);
+    p.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
+    p.eps = eps;
+}
+
+}  // namespace
+
+extern "C" {
+
+forge_status forge_wgrad_adamw(const void* X, const void* dY, float* W, void* m, void* v,
+                               int64_t M, int64_t N, int64_t K, forge_dtype in_dtype,
+                               forge_dtype state_dtype, float lr, float beta1, float beta2,
+                               float eps, float wd, int64_t step, const float* scales,
+                               forge_stream_t stream)
+{
+    if (!W || !m || !v) return FORGE_ERR_INVALID_ARG;
+    forge_status s;
+    if ((s = check_sizes(M, N, K)) != FORGE_OK) return s;
+    if ((s = check_inputs(X, dY, K, in_dtype, scales)) != FORGE_OK) return s;
+    if (state_dtype != FORGE_F32 && state_dtype != FORGE_BF16) return FORGE_ERR_UNSUPPORTED_DTYPE;
+    if ((s = check_adam(lr, beta1, beta2, eps, wd, step)) != FORGE_OK) return s;
+    Params p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.E = 1;
+    p.W = W;
+    p.s1 = m;
+    p.s2 = v;
+    p.scales = scales;
+    fill_adam(p, lr, beta1, beta2, eps, wd, step);
+    return run(X, dY, K, in_dtype, OP_ADAMW, state_dtype, false, p,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+forge_status forge_wgrad_sgdm(const void* X, const void* dY, float* W, void* mom, int64_t M,
+                              int64_t N, int64_t K, forge_dtype in_dtype, forge_dtype state_dtype,
+                              float lr, float momentum, float wd, const float* scales,
+                              forge_stream_t stream)
+{
+    if (!W || !mom) return FORGE_ERR_INVALID_ARG;
+    forge_status s;
+    if ((s = check_sizes(M, N, K)) != FORGE_OK) return s;
+    if ((s = check_inputs(X, dY, K, in_dtype, scales)) != FORGE_OK) return s;
+    if (state_dtype != FORGE_F32 && state_dtype != FORGE_BF16) return FORGE_ERR_UNSUPPORTED_DTYPE;
+    if (!finite_nonneg(lr) || !finite_nonneg(momentum) || !finite_nonneg(wd))
+        return FORGE_ERR_INVALID_ARG;
+    Params p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.E = 1;
+    p.W = W;
+    p.s1 = mom;
+    p.scales = scales;
+    p.lr = lr;
+    p.mu = momentum;
+    p.wd = wd;
+    return run(X, dY, K, in_dtype, OP_SGDM, state_dtype, false, p,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+forge_status forge_wgrad_only(const void* X, const void* dY, float* dW, int64_t M, int64_t N,
+                              int64_t K, forge_dtype in_dtype, const float* scales,
+                              forge_stream_t stream)
+{
+    if (!dW) return FORGE_ERR_INVALID_ARG;
+    forge_status s;
+    if ((s = check_sizes(M, N, K)) != FORGE_OK) return s;
+    if ((s = check_inputs(X, dY, K, in_dtype, scales)) != FORGE_OK) return s;
+    Params p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.E = 1;
+    p.W = dW;  // only for the alignment check; the kernel writes p.dW
+    p.dW = dW;
+    p.scales = scales;
+    return run(X, dY, K, in_dtype, OP_DW, FORGE_F32, false, p,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+forge_status forge_grouped_wgrad_adamw(const void* X, const void* dY, float* W, void* m, void* v,
+                                       const int32_t* offsets, int32_t E, int64_t T_max,
+                                       int64_t M, int64_t N, forge_dtype in_dtype,
+                                       forge_dtype state_dtype, float lr, float beta1, float beta2,
+                                       float eps, float wd, int64_t step, const float* scales,
+                                       forge_stream_t stream)
+{
+    if (!W || !m || !v || !offsets) return FORGE_ERR_INVALID_ARG;
+    if (E < 1 || E > kMaxExperts) return FORGE_ERR_INVALID_ARG;
+    forge_status s;
+    if ((s = check_sizes(M, N, T_max)) != FORGE_OK) return s;
+    if ((s = check_inputs(X, dY, T_max, in_dtype, scales)) != FORGE_OK) return s;
+    if (state_dtype != FORGE_F32 && state_dtype != FORGE_BF16) return FORGE_ERR_UNSUPPORTED_DTYPE;
+    if ((s = check_adam(lr, beta1, beta2, eps, wd, step)) != FORGE_OK) return s;
+    if (!aligned(offsets, 4)) return FORGE_ERR_MISALIGNED;
+    Params p{};
+    p.M = M;
+    p.N = N;
+    p.K = 0;
+    p.T_max = T_max;
+    p.offsets = offsets;
+    p.E = E;
+    p.W = W;
+    p.s1 = m;
+    p.s2 = v;
+    p.scales = scales;
+    fill_adam(p, lr, beta1, beta2, eps, wd, step);
+    return run(X, dY, T_max, in_dtype, OP_ADAMW, state_dtype, true, p,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* forge_status_string(forge_status status)
+{
+    switch (status) {
+    case FORGE_OK: return "ok";
+    case FORGE_ERR_INVALID_ARG: return "invalid argument";
+    case FORGE_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+    case FORGE_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    case FORGE_ERR_MISALIGNED: return "misaligned pointer or row stride";
+    case FORGE_ERR_CUDA: return "CUDA error";
+    case FORGE_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+forge_status forge_get_device_status(void)
+{
+    DeviceInfo* dev = nullptr;
+    forge_status st = current_device(&dev);
+    if (st != FORGE_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return FORGE_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_forge_status, sizeof v) != cudaSuccess) return FORGE_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_forge_status, &zero, sizeof zero) != cudaSuccess) return FORGE_ERR_CUDA;
+    return static_cast<forge_status>(v);
+}
+
+forge_status forge_selftest_wait_timeout(uint32_t timeout_us, forge_stream_t stream)
+{
+    if (timeout_us == 0 || timeout_us > 10000000u) return FORGE_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    forge_status st = current_device(&dev);
+    if (st != FORGE_OK) return st;
+    forge_wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<int64_t>(timeout_us) * 1000, dev->status);
+    return from_cuda(cudaGetLastError());
+}
+
+int32_t forge_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,550 @@
+// forge_kernel.cuh -- the fused weight-gradient GEMM + optimizer kernel.
+//
+// dW = X^T dY with the optimizer step applied in the tiled epilogue, so the
+// gradient lives only in tensor memory and registers (FORGE assessment PR,
+// tessera#565, opening paragraph; "What's already in tree and easy to miss":
+// dRhs = matmul(lhs, dy, transposeA=true) and K kept whole per output tile).
+//
+// Mapping onto the tensor core.  One output tile is 128 (d_out, m) x 256
+// (d_in, n).  The UMMA computes D[m][n] = sum_k dY[k][m] X[k][n], i.e. the
+// A operand is dY and the B operand is X, both token-major, so both are
+// "MN-major" (the contraction index k is the strided one).  D lives in TMEM
+// with one lane per m and one 32-bit column per n; the epilogue thread that
+// owns lane m therefore touches W[n][m] for consecutive n, and a warp's 32
+// lanes cover 32 consecutive m: every global access of the epilogue is a
+// fully coalesced 128-byte (fp32) or 64-byte (bf16) row segment.
+//
+// Roles (384 threads, one CTA per SM, persistent over a static tile list):
+//   warp 0      TMA producer: K-blocks of dY and X into a 4-stage ring
+//   warp 1      TMEM allocator; lane 0 issues tcgen05.mma into one of two
+//               128x256 fp32 accumulators (512 TMEM columns)
+//   warps 4-11  epilogue: tcgen05.ld the accumulator, apply AdamW / SGD-m /
+//               plain store, write W and the state back; two warpgroups
+//               split the 256 columns
+// Each output tile is computed by exactly one CTA over the whole K in a
+// fixed order: no split-K and no atomics, so results are bitwise
+// reproducible and independent of the schedule (P1).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "forge_ptx.cuh"
+
+namespace forge {
+
+enum InType : int { IN_BF16 = 0, IN_E4M3 = 1 };
+enum OpKind : int { OP_ADAMW = 0, OP_SGDM = 1, OP_DW = 2 };
+enum StateType : int { ST_F32 = 0, ST_BF16 = 1 };
+
+// device status word values (match forge_status)
+constexpr int kDevOk = 0;
+constexpr int kDevInvalidArg = -1;
+constexpr int kDevTimeout = -6;
+
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4;
+constexpr int kEpiWarps = 8;
+constexpr int BM = 128;  // m (d_out) per tile = UMMA M = TMEM lanes
+constexpr int BN = 256;  // n (d_in) per tile  = UMMA N = TMEM columns per accumulator
+constexpr int kStages = 4;
+constexpr int kStageA = 16384;  // BK rows x 128 m x elemsize
+constexpr int kStageB = 32768;  // BK rows x 256 n x elemsize
+constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kTmemCols = 512;  // two 256-column accumulators
+constexpr int kMaxExperts = 1024;
+constexpr int kSmemBarOffset = kStages * kStageBytes;
+constexpr int kSmemSchedOffset = kSmemBarOffset + 256;
+constexpr int kSmemBytes = kSmemSchedOffset + 4 * (2 * kMaxExperts + 2);
+constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
+
+template <int IT>
+struct InTraits;
+template <>
+struct InTraits<IN_BF16> {
+    static constexpr int esize = 2;
+    static constexpr int BK = 64;       // k rows per stage
+    static constexpr int box_mn = 64;   // elements per 128-byte swizzle row
+    static constexpr int umma_k = 16;   // k per tcgen05.mma
+    static constexpr uint32_t fmt = 1;  // bf16 (kind::f16)
+};
+template <>
+struct InTraits<IN_E4M3> {
+    static constexpr int esize = 1;
+    static constexpr int BK = 128;
+    static constexpr int box_mn = 128;
+    static constexpr int umma_k = 32;
+    static constexpr uint32_t fmt = 0;  // e4m3 (kind::f8f6f4)
+};
+
+struct Params {
+    int64_t M, N, K;         // dense sizes (K unused when grouped)
+    int64_t T_max;           // grouped: rows of the packed X / dY
+    const int32_t* offsets;  // grouped: [E+1] on the device
+    int32_t E;               // 1 when dense
+    int32_t tiles_m, tiles_n;
+    int32_t has_maps;  // 0 when there are no token rows at all (maps left unencoded)
+    float* W;
+    void* s1;  // m (AdamW) or momentum (SGD)
+    void* s2;  // v (AdamW)
+    float* dW;
+    const float* scales;  // {sX, sdY} for e4m3, else null
+    // AdamW
+    float decay;         // 1 - lr * wd
+    float b1, omb1, b2, omb2;
+    float step_size;     // lr / (1 - b1^t)
+    float inv_sqrt_bc2;  // 1 / sqrt(1 - b2^t)
+    float eps;
+    // SGD momentum
+    float lr, mu, wd;
+    int64_t timeout_ns;
+    int* status;  // device status word
+};
+
+struct Tile {
+    int32_t m0, n0;
+    int64_t k_begin, k_end;  // token rows [k_begin, k_end) of X / dY
+    int64_t pbase;           // element offset of this tile's expert block in W / m / v
+};
+
+// Static tile list.  Dense: tiles ordered m-fastest so the CTAs of one wave
+// share X column blocks in L2.  Grouped: experts sorted by token count,
+// heaviest first (stable), each contributing tiles_m * tiles_n tiles.
+struct Sched {
+    int32_t tiles_m, tiles_n, per_expert, total;
+    const int32_t* offs;   // smem copy of offsets (grouped) or null
+    const int32_t* order;  // smem expert order (grouped) or null
+    int64_t K, MN;
+
+    __device__ __forceinline__ Tile get(int32_t t) const
+    {
+        Tile r;
+        int32_t j = t / per_expert;
+        int32_t local = t - j * per_expert;
+        int32_t mt = local % tiles_m;
+        int32_t nt = local / tiles_m;
+        r.m0 = mt * BM;
+        r.n0 = nt * BN;
+        if (order) {
+            int32_t e = order[j];
+            r.k_begin = offs[e];
+            r.k_end = offs[e + 1];
+            r.pbase = static_cast<int64_t>(e) * MN;
+        } else {
+            r.k_begin = 0;
+            r.k_end = K;
+            r.pbase = 0;
+        }
+        return r;
+    }
+};
+
+// Bounded wait on an mbarrier phase.  Gives up after `timeout_ns` of
+// wall-clock time or when another role of this CTA has given up, records
+// FORGE_ERR_TIMEOUT in the device status word and returns false.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
+                                             volatile int* abort_flag, const Params& p)
+{
+    const uint32_t a = ptx::smem_addr(bar);
+    if (ptx::mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::mbar_try_wait(a, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (static_cast<int64_t>(ptx::globaltimer_ns() - t0) > p.timeout_ns) {
+                *abort_flag = 1;
+                *reinterpret_cast<volatile int*>(p.status) = kDevTimeout;
+                return false;
+            }
+        }
+    }
+}
+
+// Lane 0 waits (bounded); the outcome is broadcast to the whole warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          const Params& p, int lane)
+{
+    int ok = 0;
+    if (lane == 0) ok = wait_bounded(bar, parity, abort_flag, p) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// ------------------------------------------------------------------ epilogue
+
+template <int ST>
+struct StateIO;
+template <>
+struct StateIO<ST_F32> {
+    static __device__ __forceinline__ float ld(const void* base, int64_t i)
+    {
+        return __ldcs(static_cast<const float*>(base) + i);
+    }
+    static __device__ __forceinline__ void st(void* base, int64_t i, float x)
+    {
+        __stcs(static_cast<float*>(base) + i, x);
+    }
+};
+template <>
+struct StateIO<ST_BF16> {
+    static __device__ __forceinline__ float ld(const void* base, int64_t i)
+    {
+        unsigned short u = __ldcs(static_cast<const unsigned short*>(base) + i);
+        return __bfloat162float(__ushort_as_bfloat16(u));
+    }
+    static __device__ __forceinline__ void st(void* base, int64_t i, float x)
+    {
+        __stcs(static_cast<unsigned short*>(base) + i,
+               __bfloat16_as_ushort(__float2bfloat16_rn(x)));
+    }
+};
+
+// One thread, one m, up to 32 consecutive n (columns j < ncols), parameter
+// index of column j = idx0 + j * ldm.
+template <int OP, int ST>
+__device__ __forceinline__ void apply_chunk(const Params& p, const float (&g)[32], int64_t idx0,
+                                            int64_t ldm, int ncols)
+{
+    if constexpr (OP == OP_DW) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < ncols) __stcs(p.dW + idx0 + j * ldm, g[j]);
+    } else if constexpr (OP == OP_SGDM) {
+        float w[32], b[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < ncols) {
+                w[j] = __ldcs(p.W + idx0 + j * ldm);
+                b[j] = StateIO<ST>::ld(p.s1, idx0 + j * ldm);
+            }
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < ncols) {
+                // g' = g + wd W;  buf' = mu buf + g';  W' = W - lr buf'
+                const float g1 = fmaf(p.wd, w[j], g[j]);
+                const float b1 = fmaf(p.mu, b[j], g1);
+                const float w1 = fmaf(-p.lr, b1, w[j]);
+                __stcs(p.W + idx0 + j * ldm, w1);
+                StateIO<ST>::st(p.s1, idx0 + j * ldm, b1);
+            }
+    } else {
+        float w[32], a[32], b[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < ncols) {
+                w[j] = __ldcs(p.W + idx0 + j * ldm);
+                a[j] = StateIO<ST>::ld(p.s1, idx0 + j * ldm);
+                b[j] = StateIO<ST>::ld(p.s2, idx0 + j * ldm);
+            }
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < ncols) {
+                // m' = b1 m + (1-b1) g;  v' = b2 v + (1-b2) g^2
+                // W' = W (1 - lr wd) - (lr / bc1) m' / (sqrt(v') / sqrt(bc2) + eps)
+                const float gj = g[j];
+                const float m1 = fmaf(p.b1, a[j], p.omb1 * gj);
+                const float v1 = fmaf(p.b2, b[j], p.omb2 * (gj * gj));
+                const float den = fmaf(sqrtf(v1), p.inv_sqrt_bc2, p.eps);
+                const float w1 = fmaf(-p.step_size, m1 / den, w[j] * p.decay);
+                __stcs(p.W + idx0 + j * ldm, w1);
+                StateIO<ST>::st(p.s1, idx0 + j * ldm, m1);
+                StateIO<ST>::st(p.s2, idx0 + j * ldm, v1);
+            }
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int IT, int OP, int ST, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 1)
+    forge_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,  // dY
+                       const __grid_constant__ CUtensorMap tmB,  // X
+                       const Params p)
+{
+    using TR = InTraits<IT>;
+    constexpr int BK = TR::BK;
+    constexpr int kBoxBytes = TR::box_mn * TR::esize * BK;  // one 128-byte-wide column block
+    constexpr int kABoxes = BM / TR::box_mn;
+    constexpr int kBBoxes = BN / TR::box_mn;
+    constexpr int kKSteps = BK / TR::umma_k;
+    constexpr uint32_t kKStepBytes = TR::umma_k * 128;  // umma_k rows of 128 bytes
+    constexpr uint32_t kIdesc = ptx::make_idesc(TR::fmt, TR::fmt, true, true, BM, BN);
+    static_assert(kABoxes * kBoxBytes == kStageA && kBBoxes * kBoxBytes == kStageB, "stage size");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemBarOffset);
+    uint64_t* empty = full + kStages;
+    uint64_t* tfull = empty + kStages;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int32_t* s_offs = reinterpret_cast<int32_t*>(smem + kSmemSchedOffset);
+    int32_t* s_order = s_offs + (kMaxExperts + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&tfull[b], 1);
+            ptx::mbar_init(&tempty[b], kEpiWarps);
+        }
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0;
+        ptx::fence_mbarrier_init();
+    }
+
+    if constexpr (GROUPED) {
+        // Copy the expert offsets and validate them; rank experts by token
+        // count (descending, ties by index) without atomics.
+        for (int i = threadIdx.x; i <= p.E; i += kThreads) s_offs[i] = p.offsets[i];
+        __syncthreads();
+        __shared__ int bad;
+        if (threadIdx.x == 0) bad = 0;
+        __syncthreads();
+        for (int e = threadIdx.x; e < p.E; e += kThreads) {
+            const int32_t a = s_offs[e], b = s_offs[e + 1];
+            if (a < 0 || b < a || static_cast<int64_t>(b) > p.T_max) bad = 1;
+        }
+        __syncthreads();
+        if (bad) {
+            if (threadIdx.x == 0 && blockIdx.x == 0) *reinterpret_cast<volatile int*>(p.status) = kDevInvalidArg;
+            return;  // uniform across the CTA; nothing allocated yet
+        }
+        for (int e = threadIdx.x; e < p.E; e += kThreads) {
+            const int32_t ke = s_offs[e + 1] - s_offs[e];
+            int32_t rank = 0;
+            for (int f = 0; f < p.E; ++f) {
+                const int32_t kf = s_offs[f + 1] - s_offs[f];
+                rank += (kf > ke) || (kf == ke && f < e);
+            }
+            s_order[rank] = e;
+        }
+    }
+
+    if (warp == 0 && lane == 0 && p.has_maps) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(tmem_slot, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    Sched sc;
+    sc.tiles_m = p.tiles_m;
+    sc.tiles_n = p.tiles_n;
+    sc.per_expert = p.tiles_m * p.tiles_n;
+    sc.total = sc.per_expert * p.E;
+    sc.offs = GROUPED ? s_offs : nullptr;
+    sc.order = GROUPED ? s_order : nullptr;
+    sc.K = p.K;
+    sc.MN = p.M * p.N;
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            const uint64_t pol = ptx::policy_evict_last();
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued_mask = 0, last_parity = 0;
+            bool ok = true;
+            for (int32_t t = blockIdx.x; ok && t < sc.total; t += gridDim.x) {
+                const Tile tl = sc.get(t);
+                for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
+                    if (!wait_bounded(&empty[s], ph ^ 1u, abort_flag, p)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&full[s], kStageBytes);
+                    uint8_t* sa = smem + s * kStageBytes;
+                    uint8_t* sb = sa + kStageA;
+                    const int32_t ky = static_cast<int32_t>(k);
+#pragma unroll
+                    for (int i = 0; i < kABoxes; ++i)
+                        ptx::tma_load_2d_hint(sa + i * kBoxBytes, &tmA, &full[s],
+                                              tl.m0 + i * TR::box_mn, ky, pol);
+#pragma unroll
+                    for (int i = 0; i < kBBoxes; ++i)
+                        ptx::tma_load_2d_hint(sb + i * kBoxBytes, &tmB, &full[s],
+                                              tl.n0 + i * TR::box_mn, ky, pol);
+                    issued_mask |= 1u << s;
+                    last_parity = (last_parity & ~(1u << s)) | (ph << s);
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Wait (bounded) for this thread's copies still in flight.
+                const uint64_t t0 = ptx::globaltimer_ns();
+                for (int q = 0; q < kStages; ++q) {
+                    if (!(issued_mask & (1u << q))) continue;
+                    const uint32_t a = ptx::smem_addr(&full[q]);
+                    while (!ptx::mbar_try_wait(a, (last_parity >> q) & 1u)) {
+                        if (static_cast<int64_t>(ptx::globaltimer_ns() - t0) > p.timeout_ns)
+                            break;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------- UMMA issuer
+        // The whole warp walks the schedule; lane 0 waits on the barriers
+        // and issues the MMAs, all lanes take part in clearing rows.
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t ct = 0;  // accumulator tiles issued by this CTA
+        bool ok = true;
+        bool issued_any = false;
+        for (int32_t t = blockIdx.x; ok && t < sc.total; t += gridDim.x) {
+            const Tile tl = sc.get(t);
+            if (tl.k_end <= tl.k_begin) continue;  // no tokens: epilogue-only tile
+            const uint32_t b = ct & 1u;
+            const uint32_t aph = (ct >> 1) & 1u;
+            ok = warp_wait(&tempty[b], aph ^ 1u, abort_flag, p, lane);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint32_t d_tmem = tmem_base + b * BN;
+            uint32_t first = 1;
+            for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
+                ok = warp_wait(&full[s], ph, abort_flag, p, lane);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                if constexpr (GROUPED) {
+                    // Rows past this expert's last token belong to the next
+                    // expert (TMA zero-fills only outside the tensor), so they
+                    // are cleared in the A operand before the tensor core
+                    // reads the stage.  With MN-major 128-byte swizzle each k
+                    // row is one whole 128-byte line per column block, so a
+                    // row is cleared without undoing the swizzle.
+                    const int64_t valid = tl.k_end - k;
+                    if (valid < BK) {
+                        const int rows = BK - static_cast<int>(valid);
+                        const int units = rows * kABoxes * 8;  // 16-byte units
+                        for (int u = lane; u < units; u += 32) {
+                            const int c = u & 7;
+                            const int rb = u >> 3;
+                            const int i = rb % kABoxes;
+                            const int r = static_cast<int>(valid) + rb / kABoxes;
+                            uint4* row = reinterpret_cast<uint4*>(smem + s * kStageBytes +
+                                                                  i * kBoxBytes + r * 128);
+                            row[c] = make_uint4(0, 0, 0, 0);
+                        }
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                }
+                if (lane == 0) {
+                    const uint32_t sa = ptx::smem_addr(smem + s * kStageBytes);
+                    const uint32_t sb = sa + kStageA;
+#pragma unroll
+                    for (int ks = 0; ks < kKSteps; ++ks) {
+                        const uint64_t ad =
+                            ptx::smem_desc_sw128(sa + ks * kKStepBytes, kBoxBytes, 1024);
+                        const uint64_t bd =
+                            ptx::smem_desc_sw128(sb + ks * kKStepBytes, kBoxBytes, 1024);
+                        if constexpr (IT == IN_BF16)
+                            ptx::umma_f16(d_tmem, ad, bd, kIdesc, first ? 0u : 1u);
+                        else
+                            ptx::umma_f8(d_tmem, ad, bd, kIdesc, first ? 0u : 1u);
+                        first = 0;
+                    }
+                    ptx::umma_commit(&empty[s]);  // stage free once these MMAs are done
+                }
+                __syncwarp();
+                first = 0;
+                issued_any = true;
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) ptx::umma_commit(&tfull[b]);  // accumulator ready
+            __syncwarp();
+            ++ct;
+        }
+        if (!ok && issued_any && lane == 0) {
+            // Wait (bounded) until every MMA this thread issued is done.
+            ptx::umma_commit(drain);
+            const uint32_t a = ptx::smem_addr(drain);
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(a, 0)) {
+                if (static_cast<int64_t>(ptx::globaltimer_ns() - t0) > p.timeout_ns) break;
+            }
+        }
+        __syncwarp();
+    } else if (warp >= kEpiWarp0) {
+        // ---------------------------------------------------- epilogue
+        const int ew = warp - kEpiWarp0;
+        const int q = warp & 3;   // TMEM lane quarter this warp may access
+        const int half = ew >> 2;  // which 128 of the 256 columns
+        const int64_t ldm = p.M;
+        float gscale = 1.0f;
+        if constexpr (IT == IN_E4M3) gscale = p.scales[0] * p.scales[1];
+        uint32_t ct = 0;
+        for (int32_t t = blockIdx.x; t < sc.total; t += gridDim.x) {
+            const Tile tl = sc.get(t);
+            const bool has_acc = tl.k_end > tl.k_begin;
+            const uint32_t b = ct & 1u;
+            if (has_acc) {
+                // warp-uniform outcome: the TMEM loads below are warp-collective
+                if (!warp_wait(&tfull[b], (ct >> 1) & 1u, abort_flag, p, lane)) break;
+                ptx::tc_fence_after();
+            }
+            const int64_t m = tl.m0 + 32 * q + lane;
+            const bool m_ok = m < p.M;
+            const int64_t n_first = tl.n0 + 128 * half;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                const int64_t n = n_first + 32 * c;
+                if (n >= p.N) break;  // warp-uniform
+                float g[32];
+                if (has_acc) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(
+                        tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN + 128 * half + 32 * c,
+                        r);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) g[j] = __uint_as_float(r[j]) * gscale;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) g[j] = 0.0f;
+                }
+                const int64_t rem_n = p.N - n;
+                const int ncols = rem_n < 32 ? static_cast<int>(rem_n) : 32;
+                if (m_ok) apply_chunk<OP, ST>(p, g, tl.pbase + n * ldm + m, ldm, ncols);
+            }
+            if (has_acc) {
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&tempty[b]);
+                ++ct;
+            }
+            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace forge
