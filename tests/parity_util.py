@@ -5,12 +5,16 @@ Tolerances (the contract of the fused path):
   Both paths see identical inputs (the fp8 codes and scales), so the only
   difference is fp32 accumulation; a tighter diagnostic bound (1e-5) is
   also asserted, which any dropped k-block, tile or operand slip breaks.
-* fp32 state (m, v, momentum): elementwise |error| <= 2e-3 * rms(oracle).
-* bf16 state: the stored value must be the round-to-nearest-even bf16 of the
-  oracle's exact value, except that the other bracketing bf16 value is
-  accepted where the exact value lies within ``band`` (relative) of the
-  midpoint between them -- fp32 arithmetic on the GPU cannot decide such
-  near-ties the way fp64 does.  The count of such elements is returned.
+* fp32 state (m, v, momentum): elementwise |error| <= 2e-3 * rms(oracle);
+  a diagnostic bound |error| <= 1e-5 * rms + 2^-20 |exact| is asserted too
+  (fp32 arithmetic on the GPU sits far inside it; a wrong coefficient does
+  not).
+* bf16 state: the stored value must be the round-to-nearest-even bf16 of
+  some y with |y - exact| within that same diagnostic band, i.e. the state
+  contract applied before the rounding to storage.  Where the exact value is
+  near a rounding midpoint, fp32 arithmetic may land on the other side, so
+  the stored value may be the other bracketing neighbour; the count of such
+  elements is returned.
 * W: |error| <= 1e-2 * lr wherever |g| > 1e-2 * rms(g) (per tensor; per
   expert in the grouped call; where an expert has g = 0 the mask is
   |m_exact| > 1e-2 * rms(m_exact)).
@@ -23,7 +27,8 @@ DW_TOL = {"bf16": 2e-3, "e4m3": 3e-2}
 DW_DIAG_TOL = 1e-5
 STATE_TOL = 2e-3
 W_TOL = 1e-2
-BF16_TIE_BAND = 2.0 ** -14
+STATE_DIAG_RMS = 1e-5
+STATE_DIAG_REL = 2.0 ** -20
 
 
 def rms(x):
@@ -46,35 +51,41 @@ def check_dw(gpu, ref, kind="bf16"):
     return e
 
 
+def _band(exact):
+    exact = np.asarray(exact, np.float64)
+    return STATE_DIAG_RMS * rms(exact) + STATE_DIAG_REL * np.abs(exact)
+
+
 def check_state_f32(gpu, exact, name="state"):
     gpu = np.asarray(gpu, np.float64)
     exact = np.asarray(exact, np.float64)
+    if not gpu.size:
+        return 0.0
     bound = STATE_TOL * rms(exact)
-    err = np.max(np.abs(gpu - exact)) if gpu.size else 0.0
-    assert err <= bound, f"{name}: max |error| {err:.3e} > 2e-3*rms = {bound:.3e}"
-    return err
+    err = np.abs(gpu - exact)
+    assert err.max() <= bound, f"{name}: max |error| {err.max():.3e} > 2e-3*rms = {bound:.3e}"
+    over = err > _band(exact)
+    assert not over.any(), (f"{name}: {int(over.sum())} elements beyond the diagnostic band "
+                            f"(worst {err.max():.3e}, rms {rms(exact):.3e})")
+    return float(err.max())
 
 
-def check_state_bf16(gpu_bits, exact, name="state", band=BF16_TIE_BAND):
+def check_state_bf16(gpu_bits, exact, name="state"):
     gpu_bits = np.asarray(gpu_bits).astype(np.uint16).ravel()
     exact = np.asarray(exact, np.float64).ravel()
     rn = oracle.round_bf16(exact)
     bad = np.nonzero(gpu_bits != rn)[0]
     if bad.size == 0:
         return 0
-    g = oracle.decode(gpu_bits[bad])
-    r = oracle.decode(rn[bad])
+    band = _band(exact)[bad]
     x = exact[bad]
-    # the GPU value must be the other neighbour bracketing x ...
-    lo = np.minimum(g, r)
-    hi = np.maximum(g, r)
-    bracket = (lo <= x) & (x <= hi)
-    adjacent = np.abs(gpu_bits[bad].astype(np.int32) - rn[bad].astype(np.int32)) == 1
-    # ... and x must sit within `band` of their midpoint
-    near_tie = np.abs(x - (lo + hi) / 2) <= band * np.abs(x)
-    ok = bracket & adjacent & near_tie
-    assert ok.all(), (f"{name}: {int((~ok).sum())} bf16 values are not the rounding of the "
-                      f"exact value (first: gpu {g[~ok][:3]}, exact {x[~ok][:3]})")
+    g = oracle.decode(gpu_bits[bad])
+    lo = oracle.decode(oracle.round_bf16(x - band))
+    hi = oracle.decode(oracle.round_bf16(x + band))
+    ok = (lo <= g) & (g <= hi)
+    assert ok.all(), (f"{name}: {int((~ok).sum())} bf16 values are not the rounding of a value "
+                      f"within the band (first: gpu {g[~ok][:3]}, exact {x[~ok][:3]}, "
+                      f"rms {rms(exact):.3e})")
     return int(bad.size)
 
 

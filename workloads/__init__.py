@@ -70,8 +70,10 @@ def activations(K, width, seed, device="cpu", scale=None, dtype=torch.bfloat16):
 def with_outliers(shape, seed, device="cpu", frac=1e-3, value=20.0):
     """N(0,1) fp32 with a seeded fraction ``frac`` of entries set to +-value."""
     t = randn(shape, seed, device)
-    g = _gen(device, seed ^ 0x5A5A5A5)
     numel = t.numel()
+    if numel == 0:
+        return t
+    g = _gen(device, seed ^ 0x5A5A5A5)
     n_out = max(1, int(round(numel * frac)))
     idx = torch.randint(0, numel, (n_out,), generator=g, device=device)
     sign = torch.randint(0, 2, (n_out,), generator=g, device=device).to(torch.float32) * 2 - 1
@@ -82,7 +84,7 @@ def with_outliers(shape, seed, device="cpu", frac=1e-3, value=20.0):
 def quantize_e4m3(t: torch.Tensor):
     """Per-tensor scale s = amax / 448 and codes = RNE(t / s) in e4m3fn.
     Returns (codes, s) with s a python float (fp32 value)."""
-    amax = float(t.abs().max())
+    amax = float(t.abs().max()) if t.numel() else 0.0
     s = float(np.float32(amax / E4M3_MAX)) if amax > 0 else 1.0
     codes = (t / s).to(torch.float8_e4m3fn)
     return codes, s
