@@ -1,0 +1,392 @@
+"""Benchmark of the fused weight-gradient GEMM + AdamW step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload mlp_down|attn_proj|linear|moe|fp8]
+
+One step is one pass of the whole fused path over one batch of synthetic
+input: dW = X^T dY with the AdamW update of W, m, v in the GEMM's epilogue.
+The default workload is the Llama-style MLP down-projection (K = 8192
+tokens, d_in = 14336, d_out = 4096, bf16 X / dY, fp32 W / m / v, AdamW
+step t = 4 onward).  ``value`` is TFLOP/s = 2 M N K / (device time per step),
+with inputs resident in HBM; ``e2e`` is the same metric through the C ABI
+with pinned host buffers (host->device copies of X and dY and the
+device->host copy of the updated W inside the timed region).
+
+Multi-GPU: the path is replicated (each rank runs its own full workload, no
+collective on the data path); value sums over ranks and the time is the max
+over ranks.  ``--impl reference`` times the fp64 CPU oracle on the host cores
+on a bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "fused wgrad+AdamW TFLOP/s and % of roofline; grad_W HBM bytes (must be 0)"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 512 << 20
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except OSError:
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def profile_summary():
+    """Per-launch DRAM traffic of the fused kernel from the committed ncu summary."""
+    p = os.path.join(ROOT, "profiles", "fused_adamw_mlp_down.json")
+    try:
+        with open(p) as f:
+            return json.load(f)
+    except OSError:
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        reasons = sorted({self.NAMES[i] for s in self.samples for i in range(4)
+                          if s[2 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- workloads
+
+class Dense:
+    """One fused wgrad+AdamW call per step on a [K, N] x [K, M] problem."""
+
+    def __init__(self, wk: wl.Workload, dev, state_dtype=torch.float32):
+        self.wk = wk
+        self.dev = dev
+        K, N, M = wk.K, wk.N, wk.M
+        self.X = wl.activations(K, N, wl.seed_of(wk.name, "X"), device=dev)
+        self.D = wl.activations(K, M, wl.seed_of(wk.name, "dY"), device=dev)
+        self.W = wl.randn((N, M), wl.seed_of(wk.name, "W"), device=dev, std=0.02)
+        self.m = wl.randn((N, M), wl.seed_of(wk.name, "m"), device=dev, std=1e-3).to(state_dtype)
+        self.v = (wl.randn((N, M), wl.seed_of(wk.name, "v"), device=dev, std=1e-3) ** 2).to(
+            state_dtype)
+        self.hp = wk.adam.f32()
+        self.t = wk.first_step
+        self.flops = wk.flops
+        self.params = N * M
+        es = 4 if state_dtype == torch.float32 else 2
+        # algorithmic bytes: X and dY read once, W read+write, m and v read+write
+        self.bytes = (K * N + K * M) * 2 + N * M * (8 + 4 * es)
+
+    def step(self, X=None, D=None, stream=None):
+        import weight_grad_gemm_gb300 as fg
+        hp = self.hp
+        fg.forge_wgrad_adamw(self.X if X is None else X, self.D if D is None else D, self.W,
+                             self.m, self.v, lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps,
+                             wd=hp.wd, step=self.t, stream=stream)
+        self.t += 1
+
+
+WORKLOADS = {
+    "mlp_down": lambda dev: Dense(wl.MLP_DOWN, dev),
+    "attn_proj": lambda dev: Dense(wl.ATTN_PROJ[0], dev),
+    "linear": lambda dev: Dense(wl.LINEAR, dev),
+}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(job_X, job_D, job_W, job_m, job_v, hp, step, rows):
+    """The oracle (fp64 CPU) on `rows` output rows of the workload: the
+    contraction over all K for those rows and the AdamW step on them."""
+    import oracle
+    G = oracle.wgrad(job_X, job_D, rows=rows)
+    oracle.adamw(G, job_W[rows], job_m[rows], job_v[rows], lr=hp.lr, beta1=hp.beta1,
+                 beta2=hp.beta2, eps=hp.eps, wd=hp.wd, step=step)
+
+
+def host_copies(job):
+    import oracle
+    X = oracle.as_bits(job.X.cpu())
+    D = oracle.as_bits(job.D.cpu())
+    W = job.W.float().cpu().numpy()
+    m = job.m.float().cpu().numpy()
+    v = job.v.float().cpu().numpy()
+    return X, D, W, m, v
+
+
+def cpu_baseline(job, target_s=12.0):
+    import oracle
+    oracle.build()
+    X, D, W, m, v = host_copies(job)
+    K, N, M = job.wk.K, job.wk.N, job.wk.M
+    rows = list(range(4))
+    t0 = time.perf_counter()
+    oracle_sample(X, D, W, m, v, job.hp, job.t, rows)
+    t_cal = time.perf_counter() - t0
+    n = int(max(4, min(N, 4 * target_s / max(t_cal, 1e-3))))
+    rows = list(range(n))
+    t0 = time.perf_counter()
+    oracle_sample(X, D, W, m, v, job.hp, job.t, rows)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * n * M * K
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"{n} of {N} output rows (all {M} columns, full K={K}) of dW + AdamW, "
+                      f"fp64 C oracle with OpenMP"}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    wk = {"mlp_down": wl.MLP_DOWN, "attn_proj": wl.ATTN_PROJ[0], "linear": wl.LINEAR}[args.workload]
+    K, N, M = wk.K, wk.N, wk.M
+    hp = wk.adam.f32()
+    X = oracle.as_bits(wl.activations(K, N, wl.seed_of(wk.name, "X")))
+    D = oracle.as_bits(wl.activations(K, M, wl.seed_of(wk.name, "dY")))
+    rng = np.random.default_rng(0)
+    # state rows only for the sampled output rows (the rest is never touched)
+    total_budget_s = 150.0
+    t0 = time.perf_counter()
+    oracle_sample(X, D, (rng.standard_normal((1, M)) * 0.02).astype(np.float32),
+                  np.zeros((1, M), np.float32), np.zeros((1, M), np.float32), hp, wk.first_step,
+                  [0])
+    t1 = max(time.perf_counter() - t0, 1e-4)
+    rows_per_step = int(max(1, min(N, total_budget_s / (args.steps + args.warmup) / t1)))
+    Wr = (rng.standard_normal((rows_per_step, M)) * 0.02).astype(np.float32)
+    mr = (rng.standard_normal((rows_per_step, M)) * 1e-3).astype(np.float32)
+    vr = (rng.standard_normal((rows_per_step, M)) * 1e-3).astype(np.float32) ** 2
+    rows = list(range(rows_per_step))
+    for _ in range(args.warmup):
+        oracle_sample(X, D, Wr, mr, vr, hp, wk.first_step, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample(X, D, Wr, mr, vr, hp, wk.first_step, rows)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 2.0 * rows_per_step * M * K / dt / 1e12
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wk.name, "sample_rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_per_step} of {N} output rows per step (all {M} "
+                                   f"columns, full K={K}) of dW + AdamW"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mlp_down", choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    import weight_grad_gemm_gb300 as fg
+    fg.lib()  # fails loudly if the CUDA library is not built
+
+    job = WORKLOADS[args.workload](dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    for _ in range(args.warmup):
+        job.step()
+    torch.cuda.synchronize(dev)
+    if fg.forge_get_device_status() != fg.FORGE_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()  # evict L2 between steps (outside the timed events)
+        starts[i].record(stream)
+        job.step(stream=stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    wall = time.perf_counter() - wall0
+    time.sleep(0.2)
+    clk = clocks.stop()
+    if fg.forge_get_device_status() != fg.FORGE_OK:
+        raise RuntimeError("device status not OK after the timed region")
+
+    per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(sum(per_step_ms))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    value = job.flops * world / (ms * 1e-3) / 1e12
+
+    # end to end through the C ABI with pinned host buffers
+    Xh = job.X.cpu().pin_memory()
+    Dh = job.D.cpu().pin_memory()
+    Wh = torch.empty(job.W.shape, dtype=job.W.dtype).pin_memory()
+    Xd = torch.empty_like(job.X)
+    Dd = torch.empty_like(job.D)
+    e2e_times = []
+    for i in range(args.e2e_steps + 2):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        Xd.copy_(Xh, non_blocking=True)
+        Dd.copy_(Dh, non_blocking=True)
+        job.step(Xd, Dd, stream=stream)
+        Wh.copy_(job.W, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 2:
+            e2e_times.append(a.elapsed_time(b))
+    e2e_ms = float(np.mean(e2e_times))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = (Xh.numel() + Dh.numel()) * 2
+    d2h = Wh.numel() * 4
+
+    peaks, peak_src = load_peaks()
+    peak_tf = peaks["bf16_tflops"]
+    bw = peaks["hbm_gbs"]
+    kernel_tf = job.flops / (ms * 1e-3) / 1e12
+    t_tensor = job.flops / (peak_tf * 1e12)
+    t_hbm = job.bytes / (bw * 1e9)
+    prof = profile_summary()
+    traffic = prof.get("dram_bytes_per_launch") if prof else None
+    gradw = prof.get("grad_w_hbm_bytes") if prof else None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": job.wk.name + " AdamW fp32 state",
+                   "K": job.wk.K, "d_in": job.wk.N, "d_out": job.wk.M,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed between steps (512 MiB write); inputs+state 1.0 GB > L2"},
+        "pct_roofline": max(t_tensor, t_hbm) / (ms * 1e-3),
+        "updates_per_s": job.params * world / (ms * 1e-3),
+        "grad_w_hbm_bytes": gradw,
+        "roofline": {"bound": "tensor" if t_tensor >= t_hbm else "hbm", "achieved": kernel_tf,
+                     "peak": peak_tf, "unit": "TFLOP/s", "frac": kernel_tf / peak_tf,
+                     "peak_source": f"bf16_tflops burst, {peak_src}", "traffic": traffic},
+        "e2e": {"value": job.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(job)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -186,6 +186,14 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
         (p.dW && !aligned(p.dW, 4)))
         return FORGE_ERR_MISALIGNED;
 
+    // 4-element vector access in the epilogue: rows of whole vectors and
+    // vector-aligned bases (16 bytes for fp32, 8 bytes for bf16 state)
+    const uintptr_t va = state_dtype == FORGE_BF16 ? 8 : 16;
+    p.vec_ok = (p.M % 4 == 0) && aligned(p.W, 16) && (!p.s1 || aligned(p.s1, va)) &&
+                       (!p.s2 || aligned(p.s2, va)) && (!p.dW || aligned(p.dW, 16))
+                   ? 1
+                   : 0;
+
     CUtensorMap tmA, tmB;
     std::memset(&tmA, 0, sizeof tmA);
     std::memset(&tmB, 0, sizeof tmB);

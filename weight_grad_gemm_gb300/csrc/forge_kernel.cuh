@@ -55,7 +55,11 @@ constexpr int kTmemCols = 512;  // two 256-column accumulators
 constexpr int kMaxExperts = 1024;
 constexpr int kSmemBarOffset = kStages * kStageBytes;
 constexpr int kSmemSchedOffset = kSmemBarOffset + 256;
-constexpr int kSmemBytes = kSmemSchedOffset + 4 * (2 * kMaxExperts + 2);
+// per epilogue warp: one 16 (n) x 32 (m) fp32 chunk of the accumulator, used
+// to hand each lane four consecutive m of one n (see the epilogue)
+constexpr int kStageFloats = 16 * 32;
+constexpr int kSmemStageOffset = (kSmemSchedOffset + 4 * (2 * kMaxExperts + 2) + 127) & ~127;
+constexpr int kSmemBytes = kSmemStageOffset + kEpiWarps * kStageFloats * 4;
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
 
 template <int IT>
@@ -84,6 +88,7 @@ struct Params {
     int32_t E;               // 1 when dense
     int32_t tiles_m, tiles_n;
     int32_t has_maps;  // 0 when there are no token rows at all (maps left unencoded)
+    int32_t vec_ok;    // M % 4 == 0 and W / state / dW aligned for 4-element vectors
     float* W;
     void* s1;  // m (AdamW) or momentum (SGD)
     void* s2;  // v (AdamW)
@@ -184,72 +189,85 @@ struct StateIO<ST_F32> {
     {
         __stcs(static_cast<float*>(base) + i, x);
     }
+    // four consecutive elements starting at i (i % 4 == 0, 16-byte aligned)
+    static __device__ __forceinline__ void ld4(const void* base, int64_t i, float* o)
+    {
+        const float4 v =
+            __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(base) + i));
+        o[0] = v.x;
+        o[1] = v.y;
+        o[2] = v.z;
+        o[3] = v.w;
+    }
+    static __device__ __forceinline__ void st4(void* base, int64_t i, const float* x)
+    {
+        __stcs(reinterpret_cast<float4*>(static_cast<float*>(base) + i),
+               make_float4(x[0], x[1], x[2], x[3]));
+    }
 };
 template <>
 struct StateIO<ST_BF16> {
     static __device__ __forceinline__ float ld(const void* base, int64_t i)
     {
         unsigned short u = __ldcs(static_cast<const unsigned short*>(base) + i);
-        return __bfloat162float(__ushort_as_bfloat16(u));
+        return __uint_as_float(static_cast<uint32_t>(u) << 16);
     }
     static __device__ __forceinline__ void st(void* base, int64_t i, float x)
     {
         __stcs(static_cast<unsigned short*>(base) + i,
                __bfloat16_as_ushort(__float2bfloat16_rn(x)));
     }
+    // four consecutive bf16 (8 bytes, 8-byte aligned); bf16 widens exactly
+    static __device__ __forceinline__ void ld4(const void* base, int64_t i, float* o)
+    {
+        const uint2 u =
+            __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(base) + i));
+        o[0] = __uint_as_float(u.x << 16);
+        o[1] = __uint_as_float(u.x & 0xFFFF0000u);
+        o[2] = __uint_as_float(u.y << 16);
+        o[3] = __uint_as_float(u.y & 0xFFFF0000u);
+    }
+    static __device__ __forceinline__ void st4(void* base, int64_t i, const float* x)
+    {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]);  // round to nearest even
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(x[2], x[3]);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&lo);
+        u.y = *reinterpret_cast<const uint32_t*>(&hi);
+        __stcs(reinterpret_cast<uint2*>(static_cast<unsigned short*>(base) + i), u);
+    }
 };
 
-// One thread, one m, up to 32 consecutive n (columns j < ncols), parameter
-// index of column j = idx0 + j * ldm.
-template <int OP, int ST>
-__device__ __forceinline__ void apply_chunk(const Params& p, const float (&g)[32], int64_t idx0,
-                                            int64_t ldm, int ncols)
+// One lane's share of a 16 (n) x 32 (m) accumulator chunk: four n rows of
+// four consecutive m each; element [jj * 4 + i] is (n = 4 ns + jj, m = 4 mg + i).
+struct Chunk {
+    float g[16];
+    float w[16];
+    float a[16];  // m (AdamW) or momentum (SGD)
+    float b[16];  // v (AdamW)
+};
+
+// The optimizer step on four consecutive parameters of one row.
+template <int OP>
+__device__ __forceinline__ void step4(const Params& p, const float* g, float* w, float* a,
+                                      float* b)
 {
-    if constexpr (OP == OP_DW) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (j < ncols) __stcs(p.dW + idx0 + j * ldm, g[j]);
-    } else if constexpr (OP == OP_SGDM) {
-        float w[32], b[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (j < ncols) {
-                w[j] = __ldcs(p.W + idx0 + j * ldm);
-                b[j] = StateIO<ST>::ld(p.s1, idx0 + j * ldm);
-            }
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (j < ncols) {
-                // g' = g + wd W;  buf' = mu buf + g';  W' = W - lr buf'
-                const float g1 = fmaf(p.wd, w[j], g[j]);
-                const float b1 = fmaf(p.mu, b[j], g1);
-                const float w1 = fmaf(-p.lr, b1, w[j]);
-                __stcs(p.W + idx0 + j * ldm, w1);
-                StateIO<ST>::st(p.s1, idx0 + j * ldm, b1);
-            }
-    } else {
-        float w[32], a[32], b[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (j < ncols) {
-                w[j] = __ldcs(p.W + idx0 + j * ldm);
-                a[j] = StateIO<ST>::ld(p.s1, idx0 + j * ldm);
-                b[j] = StateIO<ST>::ld(p.s2, idx0 + j * ldm);
-            }
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (j < ncols) {
-                // m' = b1 m + (1-b1) g;  v' = b2 v + (1-b2) g^2
-                // W' = W (1 - lr wd) - (lr / bc1) m' / (sqrt(v') / sqrt(bc2) + eps)
-                const float gj = g[j];
-                const float m1 = fmaf(p.b1, a[j], p.omb1 * gj);
-                const float v1 = fmaf(p.b2, b[j], p.omb2 * (gj * gj));
-                const float den = fmaf(sqrtf(v1), p.inv_sqrt_bc2, p.eps);
-                const float w1 = fmaf(-p.step_size, m1 / den, w[j] * p.decay);
-                __stcs(p.W + idx0 + j * ldm, w1);
-                StateIO<ST>::st(p.s1, idx0 + j * ldm, m1);
-                StateIO<ST>::st(p.s2, idx0 + j * ldm, v1);
-            }
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (OP == OP_SGDM) {
+            // g' = g + wd W;  buf' = mu buf + g';  W' = W - lr buf'
+            const float g1 = fmaf(p.wd, w[i], g[i]);
+            a[i] = fmaf(p.mu, a[i], g1);
+            w[i] = fmaf(-p.lr, a[i], w[i]);
+        } else if constexpr (OP == OP_ADAMW) {
+            // m' = b1 m + (1-b1) g;  v' = b2 v + (1-b2) g^2
+            // W' = W (1 - lr wd) - (lr / bc1) m' / (sqrt(v') / sqrt(bc2) + eps)
+            const float gi = g[i];
+            a[i] = fmaf(p.b1, a[i], p.omb1 * gi);
+            b[i] = fmaf(p.b2, b[i], p.omb2 * (gi * gi));
+            const float den = fmaf(ptx::sqrt_approx(b[i]), p.inv_sqrt_bc2, p.eps);
+            w[i] = fmaf(-p.step_size * a[i], ptx::rcp_approx(den), w[i] * p.decay);
+        }
     }
 }
 
@@ -489,10 +507,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
         // ---------------------------------------------------- epilogue
+        // Warp (q, half) owns TMEM lanes 32q..32q+31 (m) and columns
+        // 128 half .. 128 half + 127 (n) of the accumulator, walked in 16-column
+        // chunks.  Each chunk goes TMEM -> registers (lane = m) -> a 2 KB smem
+        // stage -> registers again with lane (mg, ns) holding m = 4 mg .. 4 mg + 3
+        // for n = 4 ns .. 4 ns + 3, so every global access is a 16-byte (fp32)
+        // or 8-byte (bf16) vector and a warp instruction covers four 128-byte
+        // (or 64-byte) row segments.  The state loads of chunk c+1 are in
+        // flight while chunk c is updated and stored.
         const int ew = warp - kEpiWarp0;
-        const int q = warp & 3;   // TMEM lane quarter this warp may access
-        const int half = ew >> 2;  // which 128 of the 256 columns
-        const int64_t ldm = p.M;
+        const int q = warp & 3;     // TMEM lane quarter this warp may access
+        const int half = ew >> 2;   // which 128 of the 256 columns
+        const int mg = lane & 7;
+        const int ns = lane >> 3;
+        float* stg = reinterpret_cast<float*>(smem + kSmemStageOffset) + ew * kStageFloats;
+        const int64_t M = p.M;
+        const int64_t N = p.N;
         float gscale = 1.0f;
         if constexpr (IT == IN_E4M3) gscale = p.scales[0] * p.scales[1];
         uint32_t ct = 0;
@@ -505,36 +535,122 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!warp_wait(&tfull[b], (ct >> 1) & 1u, abort_flag, p, lane)) break;
                 ptx::tc_fence_after();
             }
-            const int64_t m = tl.m0 + 32 * q + lane;
-            const bool m_ok = m < p.M;
+            const int64_t mrow = tl.m0 + 32 * q + 4 * mg;  // this lane's first m
+            const int mvalid = mrow >= M ? 0 : (mrow + 4 <= M ? 4 : static_cast<int>(M - mrow));
+            const bool vec = p.vec_ok && mvalid == 4;
             const int64_t n_first = tl.n0 + 128 * half;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                const int64_t n = n_first + 32 * c;
-                if (n >= p.N) break;  // warp-uniform
-                float g[32];
-                if (has_acc) {
-                    uint32_t r[32];
-                    ptx::tmem_ld_32x32b_x32(
-                        tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN + 128 * half + 32 * c,
-                        r);
-                    ptx::tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) g[j] = __uint_as_float(r[j]) * gscale;
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) g[j] = 0.0f;
-                }
-                const int64_t rem_n = p.N - n;
-                const int ncols = rem_n < 32 ? static_cast<int>(rem_n) : 32;
-                if (m_ok) apply_chunk<OP, ST>(p, g, tl.pbase + n * ldm + m, ldm, ncols);
-            }
-            if (has_acc) {
+            const int64_t left = N - n_first;
+            const int nchunks = left <= 0 ? 0 : (left >= 128 ? 8 : static_cast<int>((left + 15) / 16));
+            const uint32_t tcol = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN + 128 * half;
+
+            auto release = [&]() {
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&tempty[b]);
-                ++ct;
+            };
+
+            auto fetch = [&](int c, Chunk& ch) {
+                if (has_acc) {
+                    uint32_t r[16];
+                    ptx::tmem_ld_32x32b_x16(tcol + 16 * c, r);
+                    ptx::tmem_ld_wait();
+                    if (c == nchunks - 1) release();  // accumulator fully read
+                    __syncwarp();  // previous chunk's stage reads are complete
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = __uint_as_float(r[j]) * gscale;
+                    __syncwarp();
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const float4 v =
+                            *reinterpret_cast<const float4*>(stg + (4 * ns + jj) * 32 + 4 * mg);
+                        ch.g[jj * 4 + 0] = v.x;
+                        ch.g[jj * 4 + 1] = v.y;
+                        ch.g[jj * 4 + 2] = v.z;
+                        ch.g[jj * 4 + 3] = v.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) ch.g[j] = 0.0f;
+                }
+                if constexpr (OP != OP_DW) {
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int64_t n = n_first + 16 * c + 4 * ns + jj;
+                        if (n >= N || mvalid == 0) continue;
+                        const int64_t idx = tl.pbase + n * M + mrow;
+                        float* w = ch.w + 4 * jj;
+                        float* a = ch.a + 4 * jj;
+                        float* bb = ch.b + 4 * jj;
+                        if (vec) {
+                            StateIO<ST_F32>::ld4(p.W, idx, w);
+                            StateIO<ST>::ld4(p.s1, idx, a);
+                            if constexpr (OP == OP_ADAMW) StateIO<ST>::ld4(p.s2, idx, bb);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                if (i < mvalid) {
+                                    w[i] = StateIO<ST_F32>::ld(p.W, idx + i);
+                                    a[i] = StateIO<ST>::ld(p.s1, idx + i);
+                                    if constexpr (OP == OP_ADAMW) bb[i] = StateIO<ST>::ld(p.s2, idx + i);
+                                }
+                        }
+                    }
+                }
+            };
+
+            auto process = [&](int c, Chunk& ch) {
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int64_t n = n_first + 16 * c + 4 * ns + jj;
+                    if (n >= N || mvalid == 0) continue;
+                    const int64_t idx = tl.pbase + n * M + mrow;
+                    float* g = ch.g + 4 * jj;
+                    if constexpr (OP == OP_DW) {
+                        if (vec) {
+                            StateIO<ST_F32>::st4(p.dW, idx, g);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                if (i < mvalid) StateIO<ST_F32>::st(p.dW, idx + i, g[i]);
+                        }
+                    } else {
+                        float* w = ch.w + 4 * jj;
+                        float* a = ch.a + 4 * jj;
+                        float* bb = ch.b + 4 * jj;
+                        step4<OP>(p, g, w, a, bb);
+                        if (vec) {
+                            StateIO<ST_F32>::st4(p.W, idx, w);
+                            StateIO<ST>::st4(p.s1, idx, a);
+                            if constexpr (OP == OP_ADAMW) StateIO<ST>::st4(p.s2, idx, bb);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                if (i < mvalid) {
+                                    StateIO<ST_F32>::st(p.W, idx + i, w[i]);
+                                    StateIO<ST>::st(p.s1, idx + i, a[i]);
+                                    if constexpr (OP == OP_ADAMW) StateIO<ST>::st(p.s2, idx + i, bb[i]);
+                                }
+                        }
+                    }
+                }
+            };
+
+            if (nchunks == 0) {
+                if (has_acc) release();
+            } else {
+                Chunk A, B;
+                fetch(0, A);
+#pragma unroll 1
+                for (int c = 0; c < nchunks; c += 2) {
+                    if (c + 1 < nchunks) fetch(c + 1, B);
+                    process(c, A);
+                    if (c + 1 < nchunks) {
+                        if (c + 2 < nchunks) fetch(c + 2, A);
+                        process(c + 1, B);
+                    }
+                }
             }
+            if (has_acc) ++ct;
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
         }
     }
