@@ -30,7 +30,7 @@ SHAPES_BF16 = [
 SHAPES_E4M3 = [(300, 528, 304), (128, 256, 128), (1, 16, 16), (0, 272, 144)]
 
 
-def bf16_inputs(K, N, M, seed, scale=None):
+def bf16_inputs(K, N, M, seed=0, scale=None):
     X = wl.activations(K, N, wl.seed_of("X", seed, K, N), scale=scale)
     D = wl.activations(K, M, wl.seed_of("dY", seed, K, M), scale=scale)
     return X, D
@@ -343,3 +343,78 @@ def test_grouped_bad_offsets_flagged_on_device(cuda_device):
     got = run_grouped(cuda_device, X, D, bad, W, m, v, step=1)
     assert fg.forge_get_device_status() == fg.FORGE_ERR_INVALID_ARG
     assert np.array_equal(got[0], W0)  # nothing written
+
+
+# ------------------------------------------------------------------ rows TMA cannot address
+
+# (K, N, M): row strides that are not multiples of 16 bytes go through the
+# cp.async loader; d_out not a multiple of 4 also exercises the scalar epilogue
+SHAPES_MISALIGNED_BF16 = [
+    (300, 264, 4100),   # dY rows 8200 B -> 8-byte copies
+    (130, 264, 302),    # dY rows 604 B -> 4-byte copies, scalar epilogue
+    (200, 4100, 136),   # X rows 8200 B
+    (77, 1002, 302),    # both operands, 4-byte copies
+    (1, 6, 10),         # one token, tiny
+]
+
+
+@pytest.mark.parametrize("K,N,M", SHAPES_MISALIGNED_BF16)
+def test_wgrad_only_misaligned_rows(cuda_device, K, N, M):
+    X, D = bf16_inputs(K, N, M, 40)
+    dW = torch.full((N, M), float("nan"), device=cuda_device)
+    fg.forge_wgrad_only(X.to(cuda_device), D.to(cuda_device), dW)
+    torch.cuda.synchronize()
+    check_dw(dW.cpu().numpy(), oracle.wgrad(X, D), "bf16")
+
+
+@pytest.mark.parametrize("state_bf16", [False, True], ids=["f32state", "bf16state"])
+@pytest.mark.parametrize("K,N,M", SHAPES_MISALIGNED_BF16)
+def test_adamw_misaligned_rows(cuda_device, K, N, M, state_bf16):
+    X, D = bf16_inputs(K, N, M, 41)
+    W, m, v = warm_state(N, M, 42, state_bf16)
+    got = run_adamw(cuda_device, X, D, W, m, v, step=5)
+    G = oracle.wgrad(X, D)
+    ref = oracle.adamw(G, W, m, v, step=5, **vars(HP))
+    check_adamw(got, ref, G, HP.lr, state_bf16)
+
+
+@pytest.mark.parametrize("K,N,M", [(256, 520, 1000), (100, 260, 4100)])
+def test_e4m3_misaligned_rows(cuda_device, K, N, M):
+    X, D, sc = e4m3_inputs(K, N, M, 43)
+    W, m, v = warm_state(N, M, 44)
+    got = run_adamw(cuda_device, X, D, W, m, v, step=2, scales=sc)
+    G = oracle.wgrad(X, D, scales=sc)
+    ref = oracle.adamw(G, W, m, v, step=2, **vars(HP))
+    check_adamw(got, ref, G, HP.lr, False)
+
+
+def test_offset_base_pointers(cuda_device):
+    # operands that start 8 bytes into an allocation: TMA needs 16-byte bases
+    K, N, M = 96, 264, 136
+    X, D = bf16_inputs(K, N, M, 45)
+    xb = torch.empty(K * N + 4, dtype=torch.bfloat16, device=cuda_device)
+    db = torch.empty(K * M + 4, dtype=torch.bfloat16, device=cuda_device)
+    Xd = xb[4:].view(K, N)
+    Dd = db[4:].view(K, M)
+    Xd.copy_(X)
+    Dd.copy_(D)
+    dW = torch.empty((N, M), device=cuda_device)
+    fg.forge_wgrad_only(Xd, Dd, dW)
+    torch.cuda.synchronize()
+    check_dw(dW.cpu().numpy(), oracle.wgrad(X, D))
+
+
+def test_grouped_misaligned_rows(cuda_device):
+    counts = [37, 0, 100, 9]
+    N, M = 264, 4100
+    X, D, off, W, m, v, sc = grouped_case(counts, N, M, 46)
+    got = run_grouped(cuda_device, X, D, off, W, m, v, step=2)
+    check_grouped(got, X, D, off, W, m, v, 2, sc, False)
+
+
+def test_two_byte_aligned_rows_are_rejected(cuda_device):
+    X, D = bf16_inputs(32, 264, 301)  # dY rows of 602 bytes
+    dW = torch.empty((264, 301), device=cuda_device)
+    with pytest.raises(fg.ForgeError) as e:
+        fg.forge_wgrad_only(X.to(cuda_device), D.to(cuda_device), dW)
+    assert e.value.status == fg.FORGE_ERR_MISALIGNED

@@ -146,24 +146,36 @@ __global__ void forge_wait_selftest_kernel(int64_t timeout_ns, int* status)
 
 forge_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FORGE_OK : FORGE_ERR_CUDA; }
 
-template <int IT>
+template <int IT, bool MAN>
 cudaError_t dispatch_op(int op, int st, bool grouped, const CUtensorMap& a, const CUtensorMap& b,
                         const Params& p, int grid, cudaStream_t s)
 {
     if (grouped) {
-        return st == ST_F32 ? launch_wgrad<IT, OP_ADAMW, ST_F32, true>(a, b, p, grid, s)
-                            : launch_wgrad<IT, OP_ADAMW, ST_BF16, true>(a, b, p, grid, s);
+        return st == ST_F32 ? launch_wgrad<IT, OP_ADAMW, ST_F32, true, MAN>(a, b, p, grid, s)
+                            : launch_wgrad<IT, OP_ADAMW, ST_BF16, true, MAN>(a, b, p, grid, s);
     }
     switch (op) {
     case OP_ADAMW:
-        return st == ST_F32 ? launch_wgrad<IT, OP_ADAMW, ST_F32, false>(a, b, p, grid, s)
-                            : launch_wgrad<IT, OP_ADAMW, ST_BF16, false>(a, b, p, grid, s);
+        return st == ST_F32 ? launch_wgrad<IT, OP_ADAMW, ST_F32, false, MAN>(a, b, p, grid, s)
+                            : launch_wgrad<IT, OP_ADAMW, ST_BF16, false, MAN>(a, b, p, grid, s);
     case OP_SGDM:
-        return st == ST_F32 ? launch_wgrad<IT, OP_SGDM, ST_F32, false>(a, b, p, grid, s)
-                            : launch_wgrad<IT, OP_SGDM, ST_BF16, false>(a, b, p, grid, s);
+        return st == ST_F32 ? launch_wgrad<IT, OP_SGDM, ST_F32, false, MAN>(a, b, p, grid, s)
+                            : launch_wgrad<IT, OP_SGDM, ST_BF16, false, MAN>(a, b, p, grid, s);
     default:
-        return launch_wgrad<IT, OP_DW, ST_F32, false>(a, b, p, grid, s);
+        return launch_wgrad<IT, OP_DW, ST_F32, false, MAN>(a, b, p, grid, s);
     }
+}
+
+// How an operand [rows, ld] of elemsize es reaches shared memory: 0 = TMA
+// (16-byte aligned base and row stride), 8 or 4 = cp.async of that width
+// (base and row stride aligned to it), -1 = not addressable.
+int operand_path(const void* base, int64_t ld, int es)
+{
+    const int64_t row = ld * es;
+    if (aligned(base, 16) && row % 16 == 0) return 0;
+    if (aligned(base, 8) && row % 8 == 0) return 8;
+    if (aligned(base, 4) && row % 4 == 0) return 4;
+    return -1;
 }
 
 // Shared tail of every entry point, after the argument checks.
@@ -177,9 +189,15 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
 
     const int es = elem_size(in_dtype);
     if (rows > 0) {
-        // TMA: 16-byte aligned bases and row strides
-        if (!aligned(X, 16) || !aligned(dY, 16) || (p.N * es) % 16 != 0 || (p.M * es) % 16 != 0)
-            return FORGE_ERR_MISALIGNED;
+        const int path_a = operand_path(dY, p.M, es);
+        const int path_b = operand_path(X, p.N, es);
+        if (path_a < 0 || path_b < 0) return FORGE_ERR_MISALIGNED;
+        p.manual_a = path_a > 0;
+        p.manual_b = path_b > 0;
+        p.gran_a = path_a;
+        p.gran_b = path_b;
+        p.gA = static_cast<const uint8_t*>(dY);
+        p.gB = static_cast<const uint8_t*>(X);
     }
     const uintptr_t sa = state_dtype == FORGE_BF16 ? 2 : 4;
     if (!aligned(p.W, 4) || (p.s1 && !aligned(p.s1, sa)) || (p.s2 && !aligned(p.s2, sa)) ||
@@ -199,8 +217,10 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
     std::memset(&tmB, 0, sizeof tmB);
     p.has_maps = rows > 0 ? 1 : 0;
     if (rows > 0) {
-        if ((st = encode_operand(&tmA, dY, in_dtype, p.M, rows)) != FORGE_OK) return st;
-        if ((st = encode_operand(&tmB, X, in_dtype, p.N, rows)) != FORGE_OK) return st;
+        if (!p.manual_a && (st = encode_operand(&tmA, dY, in_dtype, p.M, rows)) != FORGE_OK)
+            return st;
+        if (!p.manual_b && (st = encode_operand(&tmB, X, in_dtype, p.N, rows)) != FORGE_OK)
+            return st;
     }
     const int64_t tiles_m = (p.M + BM - 1) / BM;
     const int64_t tiles_n = (p.N + BN - 1) / BN;
@@ -213,9 +233,14 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
     const int grid = static_cast<int>(total < dev->sms ? total : dev->sms);
 
     const int ist = state_dtype == FORGE_BF16 ? ST_BF16 : ST_F32;
-    cudaError_t e = in_dtype == FORGE_BF16
-                        ? dispatch_op<IN_BF16>(op, ist, grouped, tmA, tmB, p, grid, stream)
-                        : dispatch_op<IN_E4M3>(op, ist, grouped, tmA, tmB, p, grid, stream);
+    const bool man = p.manual_a || p.manual_b;
+    cudaError_t e;
+    if (in_dtype == FORGE_BF16)
+        e = man ? dispatch_op<IN_BF16, true>(op, ist, grouped, tmA, tmB, p, grid, stream)
+                : dispatch_op<IN_BF16, false>(op, ist, grouped, tmA, tmB, p, grid, stream);
+    else
+        e = man ? dispatch_op<IN_E4M3, true>(op, ist, grouped, tmA, tmB, p, grid, stream)
+                : dispatch_op<IN_E4M3, false>(op, ist, grouped, tmA, tmB, p, grid, stream);
     return from_cuda(e);
 }
 

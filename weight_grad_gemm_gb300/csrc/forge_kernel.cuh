@@ -89,6 +89,12 @@ struct Params {
     int32_t tiles_m, tiles_n;
     int32_t has_maps;  // 0 when there are no token rows at all (maps left unencoded)
     int32_t vec_ok;    // M % 4 == 0 and W / state / dW aligned for 4-element vectors
+    // Operands whose rows TMA cannot address (row stride or base not a
+    // multiple of 16 bytes) are copied by the cp.async loader instead:
+    int32_t manual_a, manual_b;  // dY / X loaded by cp.async
+    int32_t gran_a, gran_b;      // cp.async width in bytes (4 or 8)
+    const uint8_t* gA;           // dY base
+    const uint8_t* gB;           // X base
     float* W;
     void* s1;  // m (AdamW) or momentum (SGD)
     void* s2;  // v (AdamW)
@@ -271,9 +277,49 @@ __device__ __forceinline__ void step4(const Params& p, const float* g, float* w,
     }
 }
 
+// ------------------------------------------------------------------ cp.async loader
+
+constexpr int kLoaderWarp0 = 2;  // warps 2 and 3
+constexpr int kLoaderThreads = 64;
+
+// Copies one operand's k-block [k0, k0 + BK) x [mn0, mn0 + tile_mn) into the
+// same 128-byte-swizzled layout TMA would produce: column block `box` (128
+// bytes of the contiguous dimension) at box * box_bytes, k row r at r * 128,
+// 16-byte chunk c of the row at (c ^ (r & 7)) * 16.  Rows at or past k_lim
+// and columns at or past mn_lim are zero-filled.
+template <int IT>
+__device__ __forceinline__ void load_block_cp_async(uint8_t* stage, const uint8_t* g, int64_t ld,
+                                                    int64_t mn0, int64_t mn_lim, int64_t k0,
+                                                    int64_t k_lim, int tile_mn, int gran, int tid)
+{
+    using TR = InTraits<IT>;
+    constexpr int BK = TR::BK;
+    constexpr int es = TR::esize;
+    constexpr int box_bytes = TR::box_mn * es * BK;
+    const int units_per_row = tile_mn * es / gran;
+    const int total = BK * units_per_row;
+    for (int u = tid; u < total; u += kLoaderThreads) {
+        const int r = u / units_per_row;
+        const int cb = (u - r * units_per_row) * gran;  // byte offset in the tile row
+        const int box = cb >> 7;
+        const int inb = cb & 127;
+        uint8_t* d = stage + box * box_bytes + r * 128 + (((inb >> 4) ^ (r & 7)) << 4) + (inb & 15);
+        const int64_t k = k0 + r;
+        const int64_t col = mn0 + cb / es;
+        int src_bytes = 0;
+        const uint8_t* src = g;
+        if (k < k_lim && col < mn_lim) {
+            const int64_t avail = (mn_lim - col) * es;
+            src_bytes = avail >= gran ? gran : static_cast<int>(avail);
+            src = g + (k * ld + col) * es;
+        }
+        ptx::cp_async(d, src, gran, src_bytes);
+    }
+}
+
 // ------------------------------------------------------------------ kernel
 
-template <int IT, int OP, int ST, bool GROUPED>
+template <int IT, int OP, int ST, bool GROUPED, bool MANUAL>
 __global__ void __launch_bounds__(kThreads, 1)
     forge_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,  // dY
                        const __grid_constant__ CUtensorMap tmB,  // X
@@ -307,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(&full[s], 1);
+            // TMA producer's arrive (+ one arrive per cp.async loader thread)
+            ptx::mbar_init(&full[s], 1 + (MANUAL ? kLoaderThreads : 0));
             ptx::mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -348,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (warp == 0 && lane == 0 && p.has_maps) {
-        ptx::prefetch_tensormap(&tmA);
-        ptx::prefetch_tensormap(&tmB);
+        if (!p.manual_a) ptx::prefetch_tensormap(&tmA);
+        if (!p.manual_b) ptx::prefetch_tensormap(&tmB);
     }
     if (warp == 1) {
         ptx::tmem_alloc(tmem_slot, kTmemCols);
@@ -373,7 +420,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
         if (lane == 0) {
+            // dY (the smaller operand, reused by every wave of tiles) is kept
+            // in L2; X column blocks are consumed within one wave.
             const uint64_t pol = ptx::policy_evict_last();
+            const bool tma_a = !(MANUAL && p.manual_a);
+            const bool tma_b = !(MANUAL && p.manual_b);
+            const uint32_t tx_bytes = (tma_a ? kStageA : 0) + (tma_b ? kStageB : 0);
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued_mask = 0, last_parity = 0;
@@ -385,18 +437,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(&full[s], kStageBytes);
+                    ptx::mbar_arrive_expect_tx(&full[s], tx_bytes);
                     uint8_t* sa = smem + s * kStageBytes;
                     uint8_t* sb = sa + kStageA;
                     const int32_t ky = static_cast<int32_t>(k);
+                    if (tma_a) {
 #pragma unroll
-                    for (int i = 0; i < kABoxes; ++i)
-                        ptx::tma_load_2d_hint(sa + i * kBoxBytes, &tmA, &full[s],
-                                              tl.m0 + i * TR::box_mn, ky, pol);
+                        for (int i = 0; i < kABoxes; ++i)
+                            ptx::tma_load_2d_hint(sa + i * kBoxBytes, &tmA, &full[s],
+                                                  tl.m0 + i * TR::box_mn, ky, pol);
+                    }
+                    if (tma_b) {
 #pragma unroll
-                    for (int i = 0; i < kBBoxes; ++i)
-                        ptx::tma_load_2d_hint(sb + i * kBoxBytes, &tmB, &full[s],
-                                              tl.n0 + i * TR::box_mn, ky, pol);
+                        for (int i = 0; i < kBBoxes; ++i)
+                            ptx::tma_load_2d(sb + i * kBoxBytes, &tmB, &full[s],
+                                             tl.n0 + i * TR::box_mn, ky);
+                    }
                     issued_mask |= 1u << s;
                     last_parity = (last_parity & ~(1u << s)) | (ph << s);
                     if (++s == kStages) {
@@ -505,6 +561,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    } else if (MANUAL && (warp == kLoaderWarp0 || warp == kLoaderWarp0 + 1)) {
+        // ---------------------------------------------------- cp.async loader
+        // Fills the operands TMA cannot address, one stage behind its own
+        // issue: after issuing stage s it waits for the copies of the
+        // previous stage, makes them visible to the tensor core (proxy
+        // fence) and arrives on that stage's full barrier.
+        const int tid = threadIdx.x - kLoaderWarp0 * 32;
+        int s = 0;
+        uint32_t ph = 0;
+        int prev = -1;
+        bool ok = true;
+        for (int32_t t = blockIdx.x; ok && t < sc.total; t += gridDim.x) {
+            const Tile tl = sc.get(t);
+            for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
+                ok = warp_wait(&empty[s], ph ^ 1u, abort_flag, p, lane);
+                if (!ok) break;
+                uint8_t* sa = smem + s * kStageBytes;
+                if (p.manual_a)
+                    load_block_cp_async<IT>(sa, p.gA, p.M, tl.m0, p.M, k, tl.k_end, BM, p.gran_a, tid);
+                if (p.manual_b)
+                    load_block_cp_async<IT>(sa + kStageA, p.gB, p.N, tl.n0, p.N, k, tl.k_end, BN,
+                                            p.gran_b, tid);
+                ptx::cp_async_commit();
+                if (prev >= 0) {
+                    ptx::cp_async_wait<1>();
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive(&full[prev]);
+                }
+                prev = s;
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        ptx::cp_async_wait<0>();
+        if (prev >= 0 && ok) {
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(&full[prev]);
+        }
     } else if (warp >= kEpiWarp0) {
         // ---------------------------------------------------- epilogue
         // Warp (q, half) owns TMEM lanes 32q..32q+31 (m) and columns

@@ -11,7 +11,7 @@ namespace forge {
 
 // Sets the kernel's shared-memory limit on the current device (once per
 // device) and launches it on `stream`.
-template <int IT, int OP, int ST, bool GROUPED>
+template <int IT, int OP, int ST, bool GROUPED, bool MANUAL>
 cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
                          int grid, cudaStream_t stream);
 
@@ -19,7 +19,7 @@ cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB, const P
 
 #define FORGE_DEFINE_LAUNCH()                                                                  \
     namespace forge {                                                                          \
-    template <int IT, int OP, int ST, bool GROUPED>                                            \
+    template <int IT, int OP, int ST, bool GROUPED, bool MANUAL>                               \
     cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,  \
                              int grid, cudaStream_t stream)                                    \
     {                                                                                          \
@@ -27,7 +27,7 @@ cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB, const P
         int dev = 0;                                                                           \
         cudaError_t e = cudaGetDevice(&dev);                                                   \
         if (e != cudaSuccess) return e;                                                        \
-        auto kern = forge_wgrad_kernel<IT, OP, ST, GROUPED>;                                   \
+        auto kern = forge_wgrad_kernel<IT, OP, ST, GROUPED, MANUAL>;                                   \
         const unsigned long long bit = 1ull << (dev & 63);                                     \
         if (!(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {                          \
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
@@ -40,6 +40,6 @@ cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB, const P
     }                                                                                          \
     }
 
-#define FORGE_INSTANTIATE(IT, OP, ST, G)                                                       \
-    template cudaError_t forge::launch_wgrad<IT, OP, ST, G>(                                   \
+#define FORGE_INSTANTIATE(IT, OP, ST, G, MAN)                                                  \
+    template cudaError_t forge::launch_wgrad<IT, OP, ST, G, MAN>(                              \
         const CUtensorMap&, const CUtensorMap&, const forge::Params&, int, cudaStream_t);

@@ -96,6 +96,25 @@ __device__ __forceinline__ uint64_t policy_evict_last()
     return p;
 }
 
+// cp.async of `bytes` (4, 8 or 16) from global to shared; only `src_bytes`
+// are read and the rest of the destination is zero-filled.
+__device__ __forceinline__ void cp_async(void* dst, const void* src, int bytes, int src_bytes)
+{
+    if (bytes == 8)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_addr(dst)),
+                     "l"(src), "r"(src_bytes)
+                     : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(dst)),
+                     "l"(src), "r"(src_bytes)
+                     : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // Make this thread's generic-proxy shared-memory writes visible to the
 // async proxy (TMA, tensor core) before a later async operation reads them.
 __device__ __forceinline__ void fence_proxy_async_smem()
