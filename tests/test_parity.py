@@ -69,10 +69,17 @@ def scales_dev(sc, dev):
     return torch.tensor(sc, dtype=torch.float32, device=dev)
 
 
+@pytest.fixture(params=["single", "pair"])
+def kernel_form(request, monkeypatch):
+    """Run a dense test on the one-CTA kernel and on the CTA-pair kernel."""
+    monkeypatch.setenv("FORGE_KERNEL", request.param)
+    return request.param
+
+
 # ------------------------------------------------------------------ dW only
 
 @pytest.mark.parametrize("K,N,M", SHAPES_BF16)
-def test_wgrad_only_bf16(cuda_device, K, N, M):
+def test_wgrad_only_bf16(cuda_device, kernel_form, K, N, M):
     X, D = bf16_inputs(K, N, M, 1)
     dW = torch.full((N, M), float("nan"), device=cuda_device)
     fg.forge_wgrad_only(X.to(cuda_device), D.to(cuda_device), dW)
@@ -87,7 +94,7 @@ def test_wgrad_only_bf16(cuda_device, K, N, M):
 
 
 @pytest.mark.parametrize("K,N,M", SHAPES_E4M3)
-def test_wgrad_only_e4m3(cuda_device, K, N, M):
+def test_wgrad_only_e4m3(cuda_device, kernel_form, K, N, M):
     X, D, sc = e4m3_inputs(K, N, M, 2)
     dW = torch.full((N, M), float("nan"), device=cuda_device)
     fg.forge_wgrad_only(X.to(cuda_device), D.to(cuda_device), dW, scales=scales_dev(sc, cuda_device))
@@ -124,7 +131,7 @@ def check_adamw(got, ref, G, lr, state_bf16):
 
 @pytest.mark.parametrize("state_bf16", [False, True], ids=["f32state", "bf16state"])
 @pytest.mark.parametrize("K,N,M", SHAPES_BF16)
-def test_adamw_bf16(cuda_device, K, N, M, state_bf16):
+def test_adamw_bf16(cuda_device, kernel_form, K, N, M, state_bf16):
     X, D = bf16_inputs(K, N, M, 3)
     W, m, v = warm_state(N, M, 4, state_bf16)
     got = run_adamw(cuda_device, X, D, W, m, v, step=4)
@@ -135,7 +142,7 @@ def test_adamw_bf16(cuda_device, K, N, M, state_bf16):
 
 @pytest.mark.parametrize("state_bf16", [False, True], ids=["f32state", "bf16state"])
 @pytest.mark.parametrize("K,N,M", SHAPES_E4M3)
-def test_adamw_e4m3(cuda_device, K, N, M, state_bf16):
+def test_adamw_e4m3(cuda_device, kernel_form, K, N, M, state_bf16):
     X, D, sc = e4m3_inputs(K, N, M, 5)
     W, m, v = warm_state(N, M, 6, state_bf16)
     got = run_adamw(cuda_device, X, D, W, m, v, step=2, scales=sc)
@@ -144,7 +151,7 @@ def test_adamw_e4m3(cuda_device, K, N, M, state_bf16):
     check_adamw(got, ref, G, HP.lr, state_bf16)
 
 
-def test_adamw_first_step_from_zero_state(cuda_device):
+def test_adamw_first_step_from_zero_state(cuda_device, kernel_form):
     # step 1 from m = v = 0 (the linear-layer workload's start)
     K, N, M = 512, 256, 256
     X, D = bf16_inputs(K, N, M, 7, scale=0.05)
@@ -157,7 +164,7 @@ def test_adamw_first_step_from_zero_state(cuda_device):
     check_adamw(got, ref, G, HP.lr, False)
 
 
-def test_linear_workload_ten_steps_resynced(cuda_device):
+def test_linear_workload_ten_steps_resynced(cuda_device, kernel_form):
     """The 10-step linear-layer workload; each step gated against the oracle
     started from the GPU's previous outputs."""
     wk = wl.LINEAR
@@ -180,7 +187,7 @@ def test_linear_workload_ten_steps_resynced(cuda_device):
 @pytest.mark.parametrize("state_bf16", [False, True], ids=["f32state", "bf16state"])
 @pytest.mark.parametrize("kind", ["bf16", "e4m3"])
 @pytest.mark.parametrize("K,N,M", [(200, 528, 304), (0, 272, 144), (1, 16, 16)])
-def test_sgdm(cuda_device, K, N, M, kind, state_bf16):
+def test_sgdm(cuda_device, kernel_form, K, N, M, kind, state_bf16):
     if kind == "bf16":
         X, D = bf16_inputs(K, N, M, 10)
         sc = None
@@ -284,7 +291,7 @@ def test_grouped_single_expert_equals_dense_bitwise(cuda_device):
 
 # ------------------------------------------------------------------ invariance (P1, no atomics)
 
-def test_bitwise_run_to_run(cuda_device):
+def test_bitwise_run_to_run(cuda_device, kernel_form):
     K, N, M = 1000, 1032, 648
     X, D = bf16_inputs(K, N, M, 17)
     W, m, v = warm_state(N, M, 18)

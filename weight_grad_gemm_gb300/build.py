@@ -22,7 +22,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libforge.so")
 
-SOURCES = ["forge_api.cu", "kernels_bf16.cu", "kernels_e4m3.cu"]
+SOURCES = ["forge_api.cu", "kernels_bf16.cu", "kernels_e4m3.cu", "kernels_pair_bf16.cu",
+           "kernels_pair_e4m3.cu"]
 HEADERS = ["forge_ptx.cuh", "forge_kernel.cuh", "forge_launch.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

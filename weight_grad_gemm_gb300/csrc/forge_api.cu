@@ -166,6 +166,34 @@ cudaError_t dispatch_op(int op, int st, bool grouped, const CUtensorMap& a, cons
     }
 }
 
+template <int IT>
+cudaError_t dispatch_pair(int op, int st, const CUtensorMap& a, const CUtensorMap& b,
+                          const Params& p, int grid, cudaStream_t s)
+{
+    switch (op) {
+    case OP_ADAMW:
+        return st == ST_F32 ? launch_wgrad_pair<IT, OP_ADAMW, ST_F32>(a, b, p, grid, s)
+                            : launch_wgrad_pair<IT, OP_ADAMW, ST_BF16>(a, b, p, grid, s);
+    case OP_SGDM:
+        return st == ST_F32 ? launch_wgrad_pair<IT, OP_SGDM, ST_F32>(a, b, p, grid, s)
+                            : launch_wgrad_pair<IT, OP_SGDM, ST_BF16>(a, b, p, grid, s);
+    default:
+        return launch_wgrad_pair<IT, OP_DW, ST_F32>(a, b, p, grid, s);
+    }
+}
+
+// Kernel form: the CTA-pair kernel serves dense calls whose operands TMA can
+// address and whose d_out exceeds one 128-row tile; FORGE_KERNEL=single or
+// =pair (read on every call) overrides the choice where both forms apply.
+bool use_pair_kernel(const Params& p, bool grouped, bool manual)
+{
+    if (grouped || manual) return false;
+    const char* e = std::getenv("FORGE_KERNEL");
+    if (e && std::strcmp(e, "single") == 0) return false;
+    if (e && std::strcmp(e, "pair") == 0) return true;
+    return p.M > BM;
+}
+
 // How an operand [rows, ld] of elemsize es reaches shared memory: 0 = TMA
 // (16-byte aligned base and row stride), 8 or 4 = cp.async of that width
 // (base and row stride aligned to it), -1 = not addressable.
@@ -222,7 +250,10 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
         if (!p.manual_b && (st = encode_operand(&tmB, X, in_dtype, p.N, rows)) != FORGE_OK)
             return st;
     }
-    const int64_t tiles_m = (p.M + BM - 1) / BM;
+    const bool man = p.manual_a || p.manual_b;
+    const bool pair = use_pair_kernel(p, grouped, man);
+    const int64_t tile_m = pair ? 2 * BM : BM;
+    const int64_t tiles_m = (p.M + tile_m - 1) / tile_m;
     const int64_t tiles_n = (p.N + BN - 1) / BN;
     const int64_t total = tiles_m * tiles_n * p.E;
     if (total <= 0 || total > INT32_MAX) return FORGE_ERR_INVALID_ARG;
@@ -230,11 +261,17 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
     p.tiles_n = static_cast<int32_t>(tiles_n);
     p.timeout_ns = wait_timeout_ns();
     p.status = dev->status;
-    const int grid = static_cast<int>(total < dev->sms ? total : dev->sms);
 
     const int ist = state_dtype == FORGE_BF16 ? ST_BF16 : ST_F32;
-    const bool man = p.manual_a || p.manual_b;
     cudaError_t e;
+    if (pair) {
+        const int64_t pairs = dev->sms / 2;
+        const int grid = static_cast<int>(2 * (total < pairs ? total : pairs));
+        e = in_dtype == FORGE_BF16 ? dispatch_pair<IN_BF16>(op, ist, tmA, tmB, p, grid, stream)
+                                   : dispatch_pair<IN_E4M3>(op, ist, tmA, tmB, p, grid, stream);
+        return from_cuda(e);
+    }
+    const int grid = static_cast<int>(total < dev->sms ? total : dev->sms);
     if (in_dtype == FORGE_BF16)
         e = man ? dispatch_op<IN_BF16, true>(op, ist, grouped, tmA, tmB, p, grid, stream)
                 : dispatch_op<IN_BF16, false>(op, ist, grouped, tmA, tmB, p, grid, stream);

@@ -123,6 +123,9 @@ struct Tile {
 // heaviest first (stable), each contributing tiles_m * tiles_n tiles.
 struct Sched {
     int32_t tiles_m, tiles_n, per_expert, total;
+    int32_t m_step;        // d_out rows per tile: 128 (one CTA) or 256 (CTA pair)
+    int32_t m_off;         // this CTA's first row within the tile (128 for the odd CTA of a pair)
+    int32_t first, step;   // this CTA's walk over the tile list: first, first + step, ...
     const int32_t* offs;   // smem copy of offsets (grouped) or null
     const int32_t* order;  // smem expert order (grouped) or null
     int64_t K, MN;
@@ -134,7 +137,7 @@ struct Sched {
         int32_t local = t - j * per_expert;
         int32_t mt = local % tiles_m;
         int32_t nt = local / tiles_m;
-        r.m0 = mt * BM;
+        r.m0 = mt * m_step + m_off;
         r.n0 = nt * BN;
         if (order) {
             int32_t e = order[j];
@@ -277,6 +280,171 @@ __device__ __forceinline__ void step4(const Params& p, const float* g, float* w,
     }
 }
 
+// ------------------------------------------------------------------ epilogue role
+
+// Epilogue warps 4..11 of one CTA.  Warp (q, half) owns TMEM lanes
+// 32q..32q+31 (m) and columns 128 half .. 128 half + 127 (n) of the
+// accumulator, walked in 16-column chunks.  Each chunk goes TMEM -> registers
+// (lane = m) -> a 2 KB smem stage -> registers again with lane (mg, ns)
+// holding m = 4 mg .. 4 mg + 3 for n = 4 ns .. 4 ns + 3, so every global access
+// is a 16-byte (fp32) or 8-byte (bf16) vector and a warp instruction covers
+// four 128-byte (or 64-byte) row segments.  The state loads of chunk c+1 are
+// in flight while chunk c is updated and stored.  `release_acc(b)` hands
+// accumulator buffer b back to the MMA issuer once it has been read.
+template <int IT, int OP, int ST, class ReleaseAcc>
+__device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, uint8_t* smem,
+                                              uint64_t* tfull, uint32_t tmem_base,
+                                              volatile int* abort_flag, int warp, int lane,
+                                              ReleaseAcc release_acc)
+{
+        // Warp (q, half) owns TMEM lanes 32q..32q+31 (m) and columns
+    // 128 half .. 128 half + 127 (n) of the accumulator, walked in 16-column
+    // chunks.  Each chunk goes TMEM -> registers (lane = m) -> a 2 KB smem
+    // stage -> registers again with lane (mg, ns) holding m = 4 mg .. 4 mg + 3
+    // for n = 4 ns .. 4 ns + 3, so every global access is a 16-byte (fp32)
+    // or 8-byte (bf16) vector and a warp instruction covers four 128-byte
+    // (or 64-byte) row segments.  The state loads of chunk c+1 are in
+    // flight while chunk c is updated and stored.
+    const int ew = warp - kEpiWarp0;
+    const int q = warp & 3;     // TMEM lane quarter this warp may access
+    const int half = ew >> 2;   // which 128 of the 256 columns
+    const int mg = lane & 7;
+    const int ns = lane >> 3;
+    float* stg = reinterpret_cast<float*>(smem + kSmemStageOffset) + ew * kStageFloats;
+    const int64_t M = p.M;
+    const int64_t N = p.N;
+    float gscale = 1.0f;
+    if constexpr (IT == IN_E4M3) gscale = p.scales[0] * p.scales[1];
+    uint32_t ct = 0;
+    for (int32_t t = sc.first; t < sc.total; t += sc.step) {
+        const Tile tl = sc.get(t);
+        const bool has_acc = tl.k_end > tl.k_begin;
+        const uint32_t b = ct & 1u;
+        if (has_acc) {
+            // warp-uniform outcome: the TMEM loads below are warp-collective
+            if (!warp_wait(&tfull[b], (ct >> 1) & 1u, abort_flag, p, lane)) break;
+            ptx::tc_fence_after();
+        }
+        const int64_t mrow = tl.m0 + 32 * q + 4 * mg;  // this lane's first m
+        const int mvalid = mrow >= M ? 0 : (mrow + 4 <= M ? 4 : static_cast<int>(M - mrow));
+        const bool vec = p.vec_ok && mvalid == 4;
+        const int64_t n_first = tl.n0 + 128 * half;
+        const int64_t left = N - n_first;
+        const int nchunks = left <= 0 ? 0 : (left >= 128 ? 8 : static_cast<int>((left + 15) / 16));
+        const uint32_t tcol = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN + 128 * half;
+
+        auto release = [&]() {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release_acc(b);
+        };
+
+        auto fetch = [&](int c, Chunk& ch) {
+            if (has_acc) {
+                uint32_t r[16];
+                ptx::tmem_ld_32x32b_x16(tcol + 16 * c, r);
+                ptx::tmem_ld_wait();
+                if (c == nchunks - 1) release();  // accumulator fully read
+                __syncwarp();  // previous chunk's stage reads are complete
+#pragma unroll
+                for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = __uint_as_float(r[j]) * gscale;
+                __syncwarp();
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float4 v =
+                        *reinterpret_cast<const float4*>(stg + (4 * ns + jj) * 32 + 4 * mg);
+                    ch.g[jj * 4 + 0] = v.x;
+                    ch.g[jj * 4 + 1] = v.y;
+                    ch.g[jj * 4 + 2] = v.z;
+                    ch.g[jj * 4 + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) ch.g[j] = 0.0f;
+            }
+            if constexpr (OP != OP_DW) {
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int64_t n = n_first + 16 * c + 4 * ns + jj;
+                    if (n >= N || mvalid == 0) continue;
+                    const int64_t idx = tl.pbase + n * M + mrow;
+                    float* w = ch.w + 4 * jj;
+                    float* a = ch.a + 4 * jj;
+                    float* bb = ch.b + 4 * jj;
+                    if (vec) {
+                        StateIO<ST_F32>::ld4(p.W, idx, w);
+                        StateIO<ST>::ld4(p.s1, idx, a);
+                        if constexpr (OP == OP_ADAMW) StateIO<ST>::ld4(p.s2, idx, bb);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (i < mvalid) {
+                                w[i] = StateIO<ST_F32>::ld(p.W, idx + i);
+                                a[i] = StateIO<ST>::ld(p.s1, idx + i);
+                                if constexpr (OP == OP_ADAMW) bb[i] = StateIO<ST>::ld(p.s2, idx + i);
+                            }
+                    }
+                }
+            }
+        };
+
+        auto process = [&](int c, Chunk& ch) {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int64_t n = n_first + 16 * c + 4 * ns + jj;
+                if (n >= N || mvalid == 0) continue;
+                const int64_t idx = tl.pbase + n * M + mrow;
+                float* g = ch.g + 4 * jj;
+                if constexpr (OP == OP_DW) {
+                    if (vec) {
+                        StateIO<ST_F32>::st4(p.dW, idx, g);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (i < mvalid) StateIO<ST_F32>::st(p.dW, idx + i, g[i]);
+                    }
+                } else {
+                    float* w = ch.w + 4 * jj;
+                    float* a = ch.a + 4 * jj;
+                    float* bb = ch.b + 4 * jj;
+                    step4<OP>(p, g, w, a, bb);
+                    if (vec) {
+                        StateIO<ST_F32>::st4(p.W, idx, w);
+                        StateIO<ST>::st4(p.s1, idx, a);
+                        if constexpr (OP == OP_ADAMW) StateIO<ST>::st4(p.s2, idx, bb);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (i < mvalid) {
+                                StateIO<ST_F32>::st(p.W, idx + i, w[i]);
+                                StateIO<ST>::st(p.s1, idx + i, a[i]);
+                                if constexpr (OP == OP_ADAMW) StateIO<ST>::st(p.s2, idx + i, bb[i]);
+                            }
+                    }
+                }
+            }
+        };
+
+        if (nchunks == 0) {
+            if (has_acc) release();
+        } else {
+            Chunk A, B;
+            fetch(0, A);
+#pragma unroll 1
+            for (int c = 0; c < nchunks; c += 2) {
+                if (c + 1 < nchunks) fetch(c + 1, B);
+                process(c, A);
+                if (c + 1 < nchunks) {
+                    if (c + 2 < nchunks) fetch(c + 2, A);
+                    process(c + 1, B);
+                }
+            }
+        }
+        if (has_acc) ++ct;
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+    }
+}
+
 // ------------------------------------------------------------------ cp.async loader
 
 constexpr int kLoaderWarp0 = 2;  // warps 2 and 3
@@ -410,6 +578,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     Sched sc;
     sc.tiles_m = p.tiles_m;
     sc.tiles_n = p.tiles_n;
+    sc.m_step = BM;
+    sc.m_off = 0;
+    sc.first = blockIdx.x;
+    sc.step = gridDim.x;
     sc.per_expert = p.tiles_m * p.tiles_n;
     sc.total = sc.per_expert * p.E;
     sc.offs = GROUPED ? s_offs : nullptr;
@@ -430,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             uint32_t issued_mask = 0, last_parity = 0;
             bool ok = true;
-            for (int32_t t = blockIdx.x; ok && t < sc.total; t += gridDim.x) {
+            for (int32_t t = sc.first; ok && t < sc.total; t += sc.step) {
                 const Tile tl = sc.get(t);
                 for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
                     if (!wait_bounded(&empty[s], ph ^ 1u, abort_flag, p)) {
@@ -483,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ct = 0;  // accumulator tiles issued by this CTA
         bool ok = true;
         bool issued_any = false;
-        for (int32_t t = blockIdx.x; ok && t < sc.total; t += gridDim.x) {
+        for (int32_t t = sc.first; ok && t < sc.total; t += sc.step) {
             const Tile tl = sc.get(t);
             if (tl.k_end <= tl.k_begin) continue;  // no tokens: epilogue-only tile
             const uint32_t b = ct & 1u;
@@ -572,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ph = 0;
         int prev = -1;
         bool ok = true;
-        for (int32_t t = blockIdx.x; ok && t < sc.total; t += gridDim.x) {
+        for (int32_t t = sc.first; ok && t < sc.total; t += sc.step) {
             const Tile tl = sc.get(t);
             for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
                 ok = warp_wait(&empty[s], ph ^ 1u, abort_flag, p, lane);
@@ -602,153 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive(&full[prev]);
         }
     } else if (warp >= kEpiWarp0) {
-        // ---------------------------------------------------- epilogue
-        // Warp (q, half) owns TMEM lanes 32q..32q+31 (m) and columns
-        // 128 half .. 128 half + 127 (n) of the accumulator, walked in 16-column
-        // chunks.  Each chunk goes TMEM -> registers (lane = m) -> a 2 KB smem
-        // stage -> registers again with lane (mg, ns) holding m = 4 mg .. 4 mg + 3
-        // for n = 4 ns .. 4 ns + 3, so every global access is a 16-byte (fp32)
-        // or 8-byte (bf16) vector and a warp instruction covers four 128-byte
-        // (or 64-byte) row segments.  The state loads of chunk c+1 are in
-        // flight while chunk c is updated and stored.
-        const int ew = warp - kEpiWarp0;
-        const int q = warp & 3;     // TMEM lane quarter this warp may access
-        const int half = ew >> 2;   // which 128 of the 256 columns
-        const int mg = lane & 7;
-        const int ns = lane >> 3;
-        float* stg = reinterpret_cast<float*>(smem + kSmemStageOffset) + ew * kStageFloats;
-        const int64_t M = p.M;
-        const int64_t N = p.N;
-        float gscale = 1.0f;
-        if constexpr (IT == IN_E4M3) gscale = p.scales[0] * p.scales[1];
-        uint32_t ct = 0;
-        for (int32_t t = blockIdx.x; t < sc.total; t += gridDim.x) {
-            const Tile tl = sc.get(t);
-            const bool has_acc = tl.k_end > tl.k_begin;
-            const uint32_t b = ct & 1u;
-            if (has_acc) {
-                // warp-uniform outcome: the TMEM loads below are warp-collective
-                if (!warp_wait(&tfull[b], (ct >> 1) & 1u, abort_flag, p, lane)) break;
-                ptx::tc_fence_after();
-            }
-            const int64_t mrow = tl.m0 + 32 * q + 4 * mg;  // this lane's first m
-            const int mvalid = mrow >= M ? 0 : (mrow + 4 <= M ? 4 : static_cast<int>(M - mrow));
-            const bool vec = p.vec_ok && mvalid == 4;
-            const int64_t n_first = tl.n0 + 128 * half;
-            const int64_t left = N - n_first;
-            const int nchunks = left <= 0 ? 0 : (left >= 128 ? 8 : static_cast<int>((left + 15) / 16));
-            const uint32_t tcol = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN + 128 * half;
-
-            auto release = [&]() {
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&tempty[b]);
-            };
-
-            auto fetch = [&](int c, Chunk& ch) {
-                if (has_acc) {
-                    uint32_t r[16];
-                    ptx::tmem_ld_32x32b_x16(tcol + 16 * c, r);
-                    ptx::tmem_ld_wait();
-                    if (c == nchunks - 1) release();  // accumulator fully read
-                    __syncwarp();  // previous chunk's stage reads are complete
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = __uint_as_float(r[j]) * gscale;
-                    __syncwarp();
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const float4 v =
-                            *reinterpret_cast<const float4*>(stg + (4 * ns + jj) * 32 + 4 * mg);
-                        ch.g[jj * 4 + 0] = v.x;
-                        ch.g[jj * 4 + 1] = v.y;
-                        ch.g[jj * 4 + 2] = v.z;
-                        ch.g[jj * 4 + 3] = v.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) ch.g[j] = 0.0f;
-                }
-                if constexpr (OP != OP_DW) {
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int64_t n = n_first + 16 * c + 4 * ns + jj;
-                        if (n >= N || mvalid == 0) continue;
-                        const int64_t idx = tl.pbase + n * M + mrow;
-                        float* w = ch.w + 4 * jj;
-                        float* a = ch.a + 4 * jj;
-                        float* bb = ch.b + 4 * jj;
-                        if (vec) {
-                            StateIO<ST_F32>::ld4(p.W, idx, w);
-                            StateIO<ST>::ld4(p.s1, idx, a);
-                            if constexpr (OP == OP_ADAMW) StateIO<ST>::ld4(p.s2, idx, bb);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                if (i < mvalid) {
-                                    w[i] = StateIO<ST_F32>::ld(p.W, idx + i);
-                                    a[i] = StateIO<ST>::ld(p.s1, idx + i);
-                                    if constexpr (OP == OP_ADAMW) bb[i] = StateIO<ST>::ld(p.s2, idx + i);
-                                }
-                        }
-                    }
-                }
-            };
-
-            auto process = [&](int c, Chunk& ch) {
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const int64_t n = n_first + 16 * c + 4 * ns + jj;
-                    if (n >= N || mvalid == 0) continue;
-                    const int64_t idx = tl.pbase + n * M + mrow;
-                    float* g = ch.g + 4 * jj;
-                    if constexpr (OP == OP_DW) {
-                        if (vec) {
-                            StateIO<ST_F32>::st4(p.dW, idx, g);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                if (i < mvalid) StateIO<ST_F32>::st(p.dW, idx + i, g[i]);
-                        }
-                    } else {
-                        float* w = ch.w + 4 * jj;
-                        float* a = ch.a + 4 * jj;
-                        float* bb = ch.b + 4 * jj;
-                        step4<OP>(p, g, w, a, bb);
-                        if (vec) {
-                            StateIO<ST_F32>::st4(p.W, idx, w);
-                            StateIO<ST>::st4(p.s1, idx, a);
-                            if constexpr (OP == OP_ADAMW) StateIO<ST>::st4(p.s2, idx, bb);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                if (i < mvalid) {
-                                    StateIO<ST_F32>::st(p.W, idx + i, w[i]);
-                                    StateIO<ST>::st(p.s1, idx + i, a[i]);
-                                    if constexpr (OP == OP_ADAMW) StateIO<ST>::st(p.s2, idx + i, bb[i]);
-                                }
-                        }
-                    }
-                }
-            };
-
-            if (nchunks == 0) {
-                if (has_acc) release();
-            } else {
-                Chunk A, B;
-                fetch(0, A);
-#pragma unroll 1
-                for (int c = 0; c < nchunks; c += 2) {
-                    if (c + 1 < nchunks) fetch(c + 1, B);
-                    process(c, A);
-                    if (c + 1 < nchunks) {
-                        if (c + 2 < nchunks) fetch(c + 2, A);
-                        process(c + 1, B);
-                    }
-                }
-            }
-            if (has_acc) ++ct;
-            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-        }
+        epilogue_role<IT, OP, ST>(p, sc, smem, tfull, tmem_base, abort_flag, warp, lane,
+                                  [&](uint32_t b) { ptx::mbar_arrive(&tempty[b]); });
     }
 
     ptx::tc_fence_before();
@@ -756,6 +783,234 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ CTA-pair kernel
+
+// Dense form on CTA pairs (clusters of two).  A pair owns a 256 (m) x 256 (n)
+// tile: CTA r loads the 128 rows m0 + 128 r .. of dY and the 128 columns
+// n0 + 128 r .. of X, and the even CTA issues tcgen05.mma.cta_group::2, which
+// reads the A half of each CTA and both B halves and leaves each CTA's 128 x
+// 256 fp32 result in its own TMEM.  A stage is therefore 32 KB per CTA
+// instead of 48 KB, so six stages fit where four did and each SM pulls a
+// third fewer operand bytes through L2 per MMA.  Each CTA runs the same
+// epilogue on its own 128 rows.  Synchronisation:
+//   full[s]   (even CTA)  its producer expects both CTAs' bytes; both CTAs'
+//                         TMA loads complete on it
+//   empty[s]  (each CTA)  the pair MMA commit arrives in both CTAs
+//   tfull[b]  (each CTA)  likewise, when accumulator b is complete
+//   tempty[b] (even CTA)  all 16 epilogue warps of the pair arrive (the odd
+//                         CTA's remotely) once accumulator b has been read
+constexpr int kPairStages = 6;
+constexpr int kPairStageA = 16384;  // this CTA's 128 rows of dY x BK
+constexpr int kPairStageB = 16384;  // this CTA's 128 columns of X x BK
+constexpr int kPairStageBytes = kPairStageA + kPairStageB;
+static_assert(kPairStages * kPairStageBytes <= kSmemBarOffset, "pair ring fits the stage area");
+
+template <int IT, int OP, int ST>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    forge_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,  // dY
+                            const __grid_constant__ CUtensorMap tmB,  // X
+                            const Params p)
+{
+    using TR = InTraits<IT>;
+    constexpr int BK = TR::BK;
+    constexpr int kBoxBytes = TR::box_mn * TR::esize * BK;
+    constexpr int kABoxes = BM / TR::box_mn;
+    constexpr int kBBoxes = (BN / 2) / TR::box_mn;
+    constexpr int kKSteps = BK / TR::umma_k;
+    constexpr uint32_t kKStepBytes = TR::umma_k * 128;
+    constexpr uint32_t kIdesc = ptx::make_idesc(TR::fmt, TR::fmt, true, true, 2 * BM, BN);
+    static_assert(kABoxes * kBoxBytes == kPairStageA && kBBoxes * kBoxBytes == kPairStageB,
+                  "stage size");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemBarOffset);
+    uint64_t* empty = full + kPairStages;
+    uint64_t* tfull = empty + kPairStages;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&tfull[b], 1);
+            ptx::mbar_init(&tempty[b], 2 * kEpiWarps);
+        }
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0;
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0 && p.has_maps) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(tmem_slot, kTmemCols);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    ptx::cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    Sched sc;
+    sc.tiles_m = p.tiles_m;  // 256-row tiles
+    sc.tiles_n = p.tiles_n;
+    sc.m_step = 2 * BM;
+    sc.m_off = static_cast<int32_t>(rank) * BM;
+    sc.first = blockIdx.x >> 1;
+    sc.step = gridDim.x >> 1;
+    sc.per_expert = p.tiles_m * p.tiles_n;
+    sc.total = sc.per_expert;
+    sc.offs = nullptr;
+    sc.order = nullptr;
+    sc.K = p.K;
+    sc.MN = p.M * p.N;
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer (both CTAs)
+        if (lane == 0) {
+            const uint64_t pol = ptx::policy_evict_last();
+            const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(&full[0]), 0);
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued_mask = 0, last_parity = 0;
+            bool ok = true;
+            for (int32_t t = sc.first; ok && t < sc.total; t += sc.step) {
+                const Tile tl = sc.get(t);
+                for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
+                    if (!wait_bounded(&empty[s], ph ^ 1u, abort_flag, p)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) ptx::mbar_arrive_expect_tx(&full[s], 2 * kPairStageBytes);
+                    uint8_t* sa = smem + s * kPairStageBytes;
+                    uint8_t* sb = sa + kPairStageA;
+                    const uint32_t bar = full0 + s * 8;
+                    const int32_t ky = static_cast<int32_t>(k);
+#pragma unroll
+                    for (int i = 0; i < kABoxes; ++i)
+                        ptx::tma_load_2d_pair_hint(sa + i * kBoxBytes, &tmA, bar,
+                                                   tl.m0 + i * TR::box_mn, ky, pol);
+#pragma unroll
+                    for (int i = 0; i < kBBoxes; ++i)
+                        ptx::tma_load_2d_pair(sb + i * kBoxBytes, &tmB, bar,
+                                              tl.n0 + static_cast<int32_t>(rank) * (BN / 2) +
+                                                  i * TR::box_mn,
+                                              ky);
+                    issued_mask |= 1u << s;
+                    last_parity = (last_parity & ~(1u << s)) | (ph << s);
+                    if (++s == kPairStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok && leader) {
+                // Wait (bounded) for the pair's copies still in flight: they
+                // all complete on the even CTA's full barriers.
+                const uint64_t t0 = ptx::globaltimer_ns();
+                for (int q = 0; q < kPairStages; ++q) {
+                    if (!(issued_mask & (1u << q))) continue;
+                    const uint32_t a = ptx::smem_addr(&full[q]);
+                    while (!ptx::mbar_try_wait(a, (last_parity >> q) & 1u)) {
+                        if (static_cast<int64_t>(ptx::globaltimer_ns() - t0) > p.timeout_ns) break;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------- pair MMA issuer (even CTA)
+        if (leader) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t ct = 0;
+            bool ok = true;
+            bool issued_any = false;
+            for (int32_t t = sc.first; ok && t < sc.total; t += sc.step) {
+                const Tile tl = sc.get(t);
+                if (tl.k_end <= tl.k_begin) continue;
+                const uint32_t b = ct & 1u;
+                const uint32_t aph = (ct >> 1) & 1u;
+                ok = warp_wait(&tempty[b], aph ^ 1u, abort_flag, p, lane);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + b * BN;
+                uint32_t first = 1;
+                for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
+                    ok = warp_wait(&full[s], ph, abort_flag, p, lane);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t sa = ptx::smem_addr(smem + s * kPairStageBytes);
+                        const uint32_t sb = sa + kPairStageA;
+#pragma unroll
+                        for (int ks = 0; ks < kKSteps; ++ks) {
+                            const uint64_t ad =
+                                ptx::smem_desc_sw128(sa + ks * kKStepBytes, kBoxBytes, 1024);
+                            const uint64_t bd =
+                                ptx::smem_desc_sw128(sb + ks * kKStepBytes, kBoxBytes, 1024);
+                            if constexpr (IT == IN_BF16)
+                                ptx::umma_f16_pair(d_tmem, ad, bd, kIdesc, first ? 0u : 1u);
+                            else
+                                ptx::umma_f8_pair(d_tmem, ad, bd, kIdesc, first ? 0u : 1u);
+                            first = 0;
+                        }
+                        ptx::umma_commit_pair(&empty[s], 0x3);  // both CTAs' stage s is free
+                    }
+                    __syncwarp();
+                    first = 0;
+                    issued_any = true;
+                    if (++s == kPairStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (lane == 0) ptx::umma_commit_pair(&tfull[b], 0x3);  // both accumulators ready
+                __syncwarp();
+                ++ct;
+            }
+            if (!ok && issued_any && lane == 0) {
+                ptx::umma_commit_pair(drain, 0x1);
+                const uint32_t a = ptx::smem_addr(drain);
+                const uint64_t t0 = ptx::globaltimer_ns();
+                while (!ptx::mbar_try_wait(a, 0)) {
+                    if (static_cast<int64_t>(ptx::globaltimer_ns() - t0) > p.timeout_ns) break;
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp >= kEpiWarp0) {
+        const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), 0);
+        epilogue_role<IT, OP, ST>(p, sc, smem, tfull, tmem_base, abort_flag, warp, lane,
+                                  [&](uint32_t b) {
+                                      if (leader)
+                                          ptx::mbar_arrive(&tempty[b]);
+                                      else
+                                          ptx::mbar_arrive_cluster(tempty0 + 8 * b);
+                                  });
+    }
+
+    ptx::tc_fence_before();
+    ptx::cluster_sync();  // no CTA leaves while its peer may still signal it
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
     }
 }
 
