@@ -144,10 +144,38 @@ class Dense:
         self.t += 1
 
 
+class Unfused:
+    """The unfused pair on the same inputs: cuBLAS bf16 matmul (fp32
+    accumulate, rounded to bf16 on output), .float(), then PyTorch's fused
+    AdamW step -- the gradient makes a round trip through HBM."""
+
+    def __init__(self, job: Dense):
+        self.job = job
+        self.W = torch.nn.Parameter(job.W.clone())
+        hp = job.hp
+        self.opt = torch.optim.AdamW([self.W], lr=hp.lr, betas=(hp.beta1, hp.beta2), eps=hp.eps,
+                                     weight_decay=hp.wd, fused=True)
+        self.opt.state[self.W] = {
+            "step": torch.tensor(float(job.t - 1), device=job.W.device),
+            "exp_avg": job.m.float().clone(), "exp_avg_sq": job.v.float().clone()}
+        self.flops = job.flops
+        self.params = job.params
+        self.bytes = job.bytes
+        self.wk = job.wk
+        self.X = job.X
+        self.D = job.D
+
+    def step(self, X=None, D=None, stream=None):
+        j = self.job
+        g = torch.matmul((j.X if X is None else X).t(), j.D if D is None else D)
+        self.W.grad = g.float()
+        self.opt.step()
+
+
 WORKLOADS = {
-    "mlp_down": lambda dev: Dense(wl.MLP_DOWN, dev),
-    "attn_proj": lambda dev: Dense(wl.ATTN_PROJ[0], dev),
-    "linear": lambda dev: Dense(wl.LINEAR, dev),
+    "mlp_down": lambda dev, st: Dense(wl.MLP_DOWN, dev, st),
+    "attn_proj": lambda dev, st: Dense(wl.ATTN_PROJ[0], dev, st),
+    "linear": lambda dev, st: Dense(wl.LINEAR, dev, st),
 }
 
 
@@ -172,16 +200,17 @@ def host_copies(job):
     return X, D, W, m, v
 
 
-def cpu_baseline(job, target_s=12.0):
+def cpu_baseline(job, target_s=15.0):
     import oracle
     oracle.build()
     X, D, W, m, v = host_copies(job)
     K, N, M = job.wk.K, job.wk.N, job.wk.M
-    rows = list(range(4))
+    oracle_sample(X, D, W, m, v, job.hp, job.t, list(range(2)))  # warm caches and threads
+    rows = list(range(32))
     t0 = time.perf_counter()
     oracle_sample(X, D, W, m, v, job.hp, job.t, rows)
     t_cal = time.perf_counter() - t0
-    n = int(max(4, min(N, 4 * target_s / max(t_cal, 1e-3))))
+    n = int(max(32, min(N, 32 * target_s / max(t_cal, 1e-3))))
     rows = list(range(n))
     t0 = time.perf_counter()
     oracle_sample(X, D, W, m, v, job.hp, job.t, rows)
@@ -250,9 +279,11 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference", "unfused"])
     ap.add_argument("--workload", default="mlp_down", choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--state", default="f32", choices=["f32", "bf16"],
+                    help="optimizer state type (default fp32, the headline workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -277,7 +308,9 @@ def main():
     import weight_grad_gemm_gb300 as fg
     fg.lib()  # fails loudly if the CUDA library is not built
 
-    job = WORKLOADS[args.workload](dev)
+    job = WORKLOADS[args.workload](dev, torch.float32 if args.state == "f32" else torch.bfloat16)
+    if args.impl == "unfused":
+        job = Unfused(job)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -334,12 +367,13 @@ def main():
         Xd.copy_(Xh, non_blocking=True)
         Dd.copy_(Dh, non_blocking=True)
         job.step(Xd, Dd, stream=stream)
-        Wh.copy_(job.W, non_blocking=True)
+        with torch.no_grad():
+            Wh.copy_(job.W, non_blocking=True)
         b.record(stream)
         b.synchronize()
         if i >= 2:
             e2e_times.append(a.elapsed_time(b))
-    e2e_ms = float(np.mean(e2e_times))
+    e2e_ms = float(np.mean(e2e_times)) if e2e_times else float("nan")
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([e2e_ms], device=dev)
@@ -360,9 +394,10 @@ def main():
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "impl": args.impl,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": job.wk.name + " AdamW fp32 state",
+        "config": {"workload": job.wk.name + f" AdamW {args.state} state",
                    "K": job.wk.K, "d_in": job.wk.N, "d_out": job.wk.M,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between steps (512 MiB write); inputs+state 1.0 GB > L2"},
@@ -374,11 +409,11 @@ def main():
                      "peak_source": f"bf16_tflops burst, {peak_src}", "traffic": traffic},
         "e2e": {"value": job.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps if args.impl == "ours" else 0,
         "clocks": clk,
         "wall_s_timed_region": wall,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.impl == "ours":
         line["cpu_baseline"] = cpu_baseline(job)
     if rank == 0:
         print(json.dumps(line), flush=True)
