@@ -69,9 +69,9 @@ def scales_dev(sc, dev):
     return torch.tensor(sc, dtype=torch.float32, device=dev)
 
 
-@pytest.fixture(params=["single", "pair"])
+@pytest.fixture(params=["single", "pair", "quad"])
 def kernel_form(request, monkeypatch):
-    """Run a dense test on the one-CTA kernel and on the CTA-pair kernel."""
+    """Run a dense test on the one-CTA kernel, on CTA pairs and on two-pair clusters."""
     monkeypatch.setenv("FORGE_KERNEL", request.param)
     return request.param
 

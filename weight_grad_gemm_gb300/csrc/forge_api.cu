@@ -24,6 +24,7 @@ namespace {
 using namespace forge;
 
 constexpr int kMaxDevices = 64;
+constexpr int32_t kDefaultRasterBand = 0;  // plain d_out-fastest order
 
 // Device status word: 0, or the first device-side error since the last read.
 __device__ int g_forge_status = 0;
@@ -97,7 +98,7 @@ forge_status current_device(DeviceInfo** out)
 // 2-D token-major operand [rows, inner] -> TMA map with 128-byte swizzled
 // boxes of (128 bytes of the inner dimension) x (k rows per stage).
 forge_status encode_operand(CUtensorMap* map, const void* base, forge_dtype dt, int64_t inner,
-                            int64_t rows)
+                            int64_t rows, int row_split = 1)
 {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
@@ -112,7 +113,8 @@ forge_status encode_operand(CUtensorMap* map, const void* base, forge_dtype dt, 
     if (!g_encode) return FORGE_ERR_CUDA;
     const int es = elem_size(dt);
     const cuuint32_t box_inner = 128 / es;
-    const cuuint32_t box_rows = dt == FORGE_BF16 ? InTraits<IN_BF16>::BK : InTraits<IN_E4M3>::BK;
+    const cuuint32_t box_rows =
+        (dt == FORGE_BF16 ? InTraits<IN_BF16>::BK : InTraits<IN_E4M3>::BK) / row_split;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * es};
     cuuint32_t box[2] = {box_inner, box_rows};
@@ -166,32 +168,47 @@ cudaError_t dispatch_op(int op, int st, bool grouped, const CUtensorMap& a, cons
     }
 }
 
-template <int IT>
+template <int IT, int NP>
 cudaError_t dispatch_pair(int op, int st, const CUtensorMap& a, const CUtensorMap& b,
-                          const Params& p, int grid, cudaStream_t s)
+                          const Params& p, int64_t grid, cudaStream_t s)
 {
     switch (op) {
     case OP_ADAMW:
-        return st == ST_F32 ? launch_wgrad_pair<IT, OP_ADAMW, ST_F32>(a, b, p, grid, s)
-                            : launch_wgrad_pair<IT, OP_ADAMW, ST_BF16>(a, b, p, grid, s);
+        return st == ST_F32 ? launch_wgrad_pair<IT, OP_ADAMW, ST_F32, NP>(a, b, p, grid, s)
+                            : launch_wgrad_pair<IT, OP_ADAMW, ST_BF16, NP>(a, b, p, grid, s);
     case OP_SGDM:
-        return st == ST_F32 ? launch_wgrad_pair<IT, OP_SGDM, ST_F32>(a, b, p, grid, s)
-                            : launch_wgrad_pair<IT, OP_SGDM, ST_BF16>(a, b, p, grid, s);
+        return st == ST_F32 ? launch_wgrad_pair<IT, OP_SGDM, ST_F32, NP>(a, b, p, grid, s)
+                            : launch_wgrad_pair<IT, OP_SGDM, ST_BF16, NP>(a, b, p, grid, s);
     default:
-        return launch_wgrad_pair<IT, OP_DW, ST_F32>(a, b, p, grid, s);
+        return launch_wgrad_pair<IT, OP_DW, ST_F32, NP>(a, b, p, grid, s);
     }
 }
 
-// Kernel form: the CTA-pair kernel serves dense calls whose operands TMA can
-// address and whose d_out exceeds one 128-row tile; FORGE_KERNEL=single or
-// =pair (read on every call) overrides the choice where both forms apply.
-bool use_pair_kernel(const Params& p, bool grouped, bool manual)
+// Kernel form: 0 = one CTA per 128 x 256 tile; 1 = CTA pairs on 256 x 256
+// tiles; 2 = clusters of two pairs (512 x 256) sharing X through multicast.
+// Pairs serve dense calls whose operands TMA can address and whose d_out
+// exceeds 128; the two-pair form moves a quarter fewer operand bytes through
+// L2 but measured no faster on GB300, so it runs only on request.
+// FORGE_KERNEL = single | pair | quad (read on every call) overrides the
+// automatic choice where that form applies.
+int kernel_form(const Params& p, bool grouped, bool manual)
 {
-    if (grouped || manual) return false;
+    if (grouped || manual) return 0;
     const char* e = std::getenv("FORGE_KERNEL");
-    if (e && std::strcmp(e, "single") == 0) return false;
-    if (e && std::strcmp(e, "pair") == 0) return true;
-    return p.M > BM;
+    if (e && std::strcmp(e, "single") == 0) return 0;
+    if (e && std::strcmp(e, "pair") == 0) return 1;
+    if (e && std::strcmp(e, "quad") == 0) return 2;
+    return p.M > BM ? 1 : 0;
+}
+
+// d_out tiles per raster band.  FORGE_RASTER_BAND (read on every call)
+// overrides the default; 0 or a value >= tiles_m means plain d_out-fastest.
+int32_t raster_band(int32_t tiles_m)
+{
+    int32_t band = kDefaultRasterBand;
+    if (const char* e = std::getenv("FORGE_RASTER_BAND")) band = std::atoi(e);
+    if (band <= 0 || band > tiles_m) band = tiles_m;
+    return band;
 }
 
 // How an operand [rows, ld] of elemsize es reaches shared memory: 0 = TMA
@@ -240,6 +257,8 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
                    ? 1
                    : 0;
 
+    const bool man = p.manual_a || p.manual_b;
+    const int form = kernel_form(p, grouped, man);
     CUtensorMap tmA, tmB;
     std::memset(&tmA, 0, sizeof tmA);
     std::memset(&tmB, 0, sizeof tmB);
@@ -247,28 +266,34 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
     if (rows > 0) {
         if (!p.manual_a && (st = encode_operand(&tmA, dY, in_dtype, p.M, rows)) != FORGE_OK)
             return st;
-        if (!p.manual_b && (st = encode_operand(&tmB, X, in_dtype, p.N, rows)) != FORGE_OK)
+        // two pairs fetch half of each X box's k rows apiece
+        if (!p.manual_b &&
+            (st = encode_operand(&tmB, X, in_dtype, p.N, rows, form == 2 ? 2 : 1)) != FORGE_OK)
             return st;
     }
-    const bool man = p.manual_a || p.manual_b;
-    const bool pair = use_pair_kernel(p, grouped, man);
-    const int64_t tile_m = pair ? 2 * BM : BM;
+    const int64_t tile_m = form == 2 ? 4 * BM : (form == 1 ? 2 * BM : BM);
     const int64_t tiles_m = (p.M + tile_m - 1) / tile_m;
     const int64_t tiles_n = (p.N + BN - 1) / BN;
     const int64_t total = tiles_m * tiles_n * p.E;
     if (total <= 0 || total > INT32_MAX) return FORGE_ERR_INVALID_ARG;
     p.tiles_m = static_cast<int32_t>(tiles_m);
     p.tiles_n = static_cast<int32_t>(tiles_n);
+    p.raster_band = raster_band(p.tiles_m);
     p.timeout_ns = wait_timeout_ns();
     p.status = dev->status;
 
     const int ist = state_dtype == FORGE_BF16 ? ST_BF16 : ST_F32;
     cudaError_t e;
-    if (pair) {
-        const int64_t pairs = dev->sms / 2;
-        const int grid = static_cast<int>(2 * (total < pairs ? total : pairs));
-        e = in_dtype == FORGE_BF16 ? dispatch_pair<IN_BF16>(op, ist, tmA, tmB, p, grid, stream)
-                                   : dispatch_pair<IN_E4M3>(op, ist, tmA, tmB, p, grid, stream);
+    if (form > 0) {
+        // the launcher sizes the grid from the resident-cluster limit
+        if (form == 1)
+            e = in_dtype == FORGE_BF16
+                    ? dispatch_pair<IN_BF16, 1>(op, ist, tmA, tmB, p, total, stream)
+                    : dispatch_pair<IN_E4M3, 1>(op, ist, tmA, tmB, p, total, stream);
+        else
+            e = in_dtype == FORGE_BF16
+                    ? dispatch_pair<IN_BF16, 2>(op, ist, tmA, tmB, p, total, stream)
+                    : dispatch_pair<IN_E4M3, 2>(op, ist, tmA, tmB, p, total, stream);
         return from_cuda(e);
     }
     const int grid = static_cast<int>(total < dev->sms ? total : dev->sms);

@@ -87,6 +87,7 @@ struct Params {
     const int32_t* offsets;  // grouped: [E+1] on the device
     int32_t E;               // 1 when dense
     int32_t tiles_m, tiles_n;
+    int32_t raster_band;  // d_out tiles per raster band, 1 <= raster_band <= tiles_m
     int32_t has_maps;  // 0 when there are no token rows at all (maps left unencoded)
     int32_t vec_ok;    // M % 4 == 0 and W / state / dW aligned for 4-element vectors
     // Operands whose rows TMA cannot address (row stride or base not a
@@ -126,6 +127,7 @@ struct Sched {
     int32_t m_step;        // d_out rows per tile: 128 (one CTA) or 256 (CTA pair)
     int32_t m_off;         // this CTA's first row within the tile (128 for the odd CTA of a pair)
     int32_t first, step;   // this CTA's walk over the tile list: first, first + step, ...
+    int32_t band;          // d_out tiles per raster band (tiles_m: plain m-fastest order)
     const int32_t* offs;   // smem copy of offsets (grouped) or null
     const int32_t* order;  // smem expert order (grouped) or null
     int64_t K, MN;
@@ -135,8 +137,16 @@ struct Sched {
         Tile r;
         int32_t j = t / per_expert;
         int32_t local = t - j * per_expert;
-        int32_t mt = local % tiles_m;
-        int32_t nt = local / tiles_m;
+        // Raster: bands of `band` d_out tiles; within a band, d_out fastest,
+        // then across all d_in tiles.  A wave of tiles then touches only the
+        // band's dY columns, which stay in L2 while the band lasts.
+        const int32_t per_band = band * tiles_n;
+        const int32_t g = local / per_band;
+        const int32_t within = local - g * per_band;
+        const int32_t rows_left = tiles_m - g * band;
+        const int32_t gsz = rows_left < band ? rows_left : band;
+        int32_t mt = g * band + within % gsz;
+        int32_t nt = within / gsz;
         r.m0 = mt * m_step + m_off;
         r.n0 = nt * BN;
         if (order) {
@@ -582,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sc.m_off = 0;
     sc.first = blockIdx.x;
     sc.step = gridDim.x;
+    sc.band = p.raster_band;
     sc.per_expert = p.tiles_m * p.tiles_n;
     sc.total = sc.per_expert * p.E;
     sc.offs = GROUPED ? s_offs : nullptr;
@@ -788,18 +799,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ CTA-pair kernel
 
-// Dense form on CTA pairs (clusters of two).  A pair owns a 256 (m) x 256 (n)
-// tile: CTA r loads the 128 rows m0 + 128 r .. of dY and the 128 columns
+// Dense form on CTA pairs.  A pair owns a 256 (m) x 256 (n) tile: CTA r of
+// the pair loads the 128 rows m0 + 128 r .. of dY and the 128 columns
 // n0 + 128 r .. of X, and the even CTA issues tcgen05.mma.cta_group::2, which
 // reads the A half of each CTA and both B halves and leaves each CTA's 128 x
 // 256 fp32 result in its own TMEM.  A stage is therefore 32 KB per CTA
 // instead of 48 KB, so six stages fit where four did and each SM pulls a
 // third fewer operand bytes through L2 per MMA.  Each CTA runs the same
-// epilogue on its own 128 rows.  Synchronisation:
-//   full[s]   (even CTA)  its producer expects both CTAs' bytes; both CTAs'
-//                         TMA loads complete on it
-//   empty[s]  (each CTA)  the pair MMA commit arrives in both CTAs
-//   tfull[b]  (each CTA)  likewise, when accumulator b is complete
+// epilogue on its own 128 rows.
+//
+// With NPAIR = 2 a cluster holds two pairs stacked along d_out (a 512 x 256
+// tile) that need the same X columns: the CTA of each pair that holds B half
+// r fetches half of that half's k rows and multicasts them to its
+// counterpart in the other pair, so L2 delivers a quarter fewer bytes per SM.
+//
+// Synchronisation (per pair unless noted):
+//   full[s]   (even CTA)  its producer expects the 64 KB landing in the pair;
+//                         every load into the pair completes on it
+//   empty[s]  (each CTA)  every pair's MMA commit arrives in every CTA of the
+//                         cluster (a CTA's stage also receives the other
+//                         pair's multicast, so all pairs must be done with it)
+//   tfull[b]  (each CTA)  the pair's MMA commit, when accumulator b is complete
 //   tempty[b] (even CTA)  all 16 epilogue warps of the pair arrive (the odd
 //                         CTA's remotely) once accumulator b has been read
 constexpr int kPairStages = 6;
@@ -808,12 +828,13 @@ constexpr int kPairStageB = 16384;  // this CTA's 128 columns of X x BK
 constexpr int kPairStageBytes = kPairStageA + kPairStageB;
 static_assert(kPairStages * kPairStageBytes <= kSmemBarOffset, "pair ring fits the stage area");
 
-template <int IT, int OP, int ST>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <int IT, int OP, int ST, int NPAIR>
+__global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
     forge_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,  // dY
-                            const __grid_constant__ CUtensorMap tmB,  // X
+                            const __grid_constant__ CUtensorMap tmB,  // X, boxes of BK / NPAIR rows
                             const Params p)
 {
+    static_assert(NPAIR == 1 || NPAIR == 2, "one or two pairs per cluster");
     using TR = InTraits<IT>;
     constexpr int BK = TR::BK;
     constexpr int kBoxBytes = TR::box_mn * TR::esize * BK;
@@ -838,13 +859,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = ptx::cluster_ctarank();
+    const uint32_t crank = ptx::cluster_ctarank();
+    const uint32_t rank = crank & 1u;         // position in the pair
+    const uint32_t pair_id = crank >> 1;      // pair within the cluster
+    const uint32_t lead_rank = crank & ~1u;   // the pair's even CTA
     const bool leader = rank == 0;
+    constexpr uint16_t kAllMask = static_cast<uint16_t>((1u << (2 * NPAIR)) - 1u);
+    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * pair_id));
+    // CTAs holding the same B half in every pair of the cluster
+    const uint16_t b_mask = static_cast<uint16_t>(NPAIR == 2 ? (0x5u << rank) : (1u << crank));
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPairStages; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&empty[s], NPAIR);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&tfull[b], 1);
@@ -863,17 +891,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::tmem_relinquish_pair();
     }
     ptx::tc_fence_before();
-    ptx::cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+    ptx::cluster_sync();  // all barriers of the cluster initialised, TMEM allocated
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     Sched sc;
-    sc.tiles_m = p.tiles_m;  // 256-row tiles
+    sc.tiles_m = p.tiles_m;  // 256 * NPAIR-row tiles
     sc.tiles_n = p.tiles_n;
-    sc.m_step = 2 * BM;
-    sc.m_off = static_cast<int32_t>(rank) * BM;
-    sc.first = blockIdx.x >> 1;
-    sc.step = gridDim.x >> 1;
+    sc.m_step = 2 * NPAIR * BM;
+    sc.m_off = static_cast<int32_t>(crank) * BM;
+    sc.first = blockIdx.x / (2 * NPAIR);
+    sc.step = gridDim.x / (2 * NPAIR);
+    sc.band = p.raster_band;
     sc.per_expert = p.tiles_m * p.tiles_n;
     sc.total = sc.per_expert;
     sc.offs = nullptr;
@@ -885,7 +914,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------- TMA producer (both CTAs)
         if (lane == 0) {
             const uint64_t pol = ptx::policy_evict_last();
-            const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(&full[0]), 0);
+            const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(&full[0]), lead_rank);
+            constexpr int kBRows = BK / NPAIR;  // k rows of each B box this CTA fetches
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued_mask = 0, last_parity = 0;
@@ -906,12 +936,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < kABoxes; ++i)
                         ptx::tma_load_2d_pair_hint(sa + i * kBoxBytes, &tmA, bar,
                                                    tl.m0 + i * TR::box_mn, ky, pol);
+                    const int32_t nb = tl.n0 + static_cast<int32_t>(rank) * (BN / 2);
 #pragma unroll
-                    for (int i = 0; i < kBBoxes; ++i)
-                        ptx::tma_load_2d_pair(sb + i * kBoxBytes, &tmB, bar,
-                                              tl.n0 + static_cast<int32_t>(rank) * (BN / 2) +
-                                                  i * TR::box_mn,
-                                              ky);
+                    for (int i = 0; i < kBBoxes; ++i) {
+                        if constexpr (NPAIR == 1) {
+                            ptx::tma_load_2d_pair(sb + i * kBoxBytes, &tmB, bar, nb + i * TR::box_mn, ky);
+                        } else {
+                            // rows [pair_id * kBRows, +kBRows) of this B box, to both pairs
+                            const int r0 = static_cast<int>(pair_id) * kBRows;
+                            ptx::tma_load_2d_pair_mc(sb + i * kBoxBytes + r0 * 128, &tmB, bar,
+                                                     nb + i * TR::box_mn, ky + r0, b_mask);
+                        }
+                    }
                     issued_mask |= 1u << s;
                     last_parity = (last_parity & ~(1u << s)) | (ph << s);
                     if (++s == kPairStages) {
@@ -970,7 +1006,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 ptx::umma_f8_pair(d_tmem, ad, bd, kIdesc, first ? 0u : 1u);
                             first = 0;
                         }
-                        ptx::umma_commit_pair(&empty[s], 0x3);  // both CTAs' stage s is free
+                        // stage s of every CTA that received this pair's loads is free
+                        ptx::umma_commit_pair(&empty[s], kAllMask);
                     }
                     __syncwarp();
                     first = 0;
@@ -981,12 +1018,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                if (lane == 0) ptx::umma_commit_pair(&tfull[b], 0x3);  // both accumulators ready
+                if (lane == 0) ptx::umma_commit_pair(&tfull[b], pair_mask);  // both accumulators ready
                 __syncwarp();
                 ++ct;
             }
             if (!ok && issued_any && lane == 0) {
-                ptx::umma_commit_pair(drain, 0x1);
+                ptx::umma_commit_pair(drain, static_cast<uint16_t>(1u << crank));
                 const uint32_t a = ptx::smem_addr(drain);
                 const uint64_t t0 = ptx::globaltimer_ns();
                 while (!ptx::mbar_try_wait(a, 0)) {
@@ -996,7 +1033,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
         }
     } else if (warp >= kEpiWarp0) {
-        const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), 0);
+        const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), lead_rank);
         epilogue_role<IT, OP, ST>(p, sc, smem, tfull, tmem_base, abort_flag, warp, lane,
                                   [&](uint32_t b) {
                                       if (leader)
@@ -1007,7 +1044,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     ptx::tc_fence_before();
-    ptx::cluster_sync();  // no CTA leaves while its peer may still signal it
+    ptx::cluster_sync();  // no CTA leaves while another may still signal it
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc_pair(tmem_base, kTmemCols);

@@ -15,39 +15,50 @@ template <int IT, int OP, int ST, bool GROUPED, bool MANUAL>
 cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
                          int grid, cudaStream_t stream);
 
-// Same for the CTA-pair kernel (grid: an even number of CTAs).
-template <int IT, int OP, int ST>
+// Same for the CTA-pair kernels.  The grid is sized from the number of
+// clusters of 2 * NPAIR CTAs that can be resident at once (a cluster must fit
+// in one GPC), never more than `total_tiles` clusters.
+template <int IT, int OP, int ST, int NPAIR>
 cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
-                              int grid, cudaStream_t stream);
+                              int64_t total_tiles, cudaStream_t stream);
 
 }  // namespace forge
 
 #define FORGE_DEFINE_LAUNCH_PAIR()                                                             \
     namespace forge {                                                                          \
-    template <int IT, int OP, int ST>                                                          \
+    template <int IT, int OP, int ST, int NPAIR>                                               \
     cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,              \
-                                  const Params& p, int grid, cudaStream_t stream)              \
+                                  const Params& p, int64_t total_tiles, cudaStream_t stream)   \
     {                                                                                          \
-        static unsigned long long attr_done = 0;                                               \
+        static int max_clusters[64] = {0};                                                     \
         int dev = 0;                                                                           \
         cudaError_t e = cudaGetDevice(&dev);                                                   \
         if (e != cudaSuccess) return e;                                                        \
-        auto kern = forge_wgrad_pair_kernel<IT, OP, ST>;                                       \
-        const unsigned long long bit = 1ull << (dev & 63);                                     \
-        if (!(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {                          \
+        auto kern = forge_wgrad_pair_kernel<IT, OP, ST, NPAIR>;                                \
+        int& mc = max_clusters[dev & 63];                                                      \
+        if (__atomic_load_n(&mc, __ATOMIC_ACQUIRE) == 0) {                                     \
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
                                      kSmemAlloc);                                              \
             if (e != cudaSuccess) return e;                                                    \
-            __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);                              \
+            cudaLaunchConfig_t cfg = {};                                                       \
+            cfg.gridDim = dim3(2 * NPAIR, 1, 1);                                               \
+            cfg.blockDim = dim3(kThreads, 1, 1);                                               \
+            cfg.dynamicSmemBytes = kSmemAlloc;                                                 \
+            int n = 0;                                                                         \
+            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);                                \
+            if (e != cudaSuccess) return e;                                                    \
+            if (n < 1) return cudaErrorInvalidConfiguration;                                   \
+            __atomic_store_n(&mc, n, __ATOMIC_RELEASE);                                        \
         }                                                                                      \
-        kern<<<grid, kThreads, kSmemAlloc, stream>>>(tmA, tmB, p);                             \
+        const int64_t nc = total_tiles < mc ? total_tiles : mc;                                \
+        kern<<<static_cast<int>(2 * NPAIR * nc), kThreads, kSmemAlloc, stream>>>(tmA, tmB, p); \
         return cudaGetLastError();                                                             \
     }                                                                                          \
     }
 
-#define FORGE_INSTANTIATE_PAIR(IT, OP, ST)                                                     \
-    template cudaError_t forge::launch_wgrad_pair<IT, OP, ST>(                                 \
-        const CUtensorMap&, const CUtensorMap&, const forge::Params&, int, cudaStream_t);
+#define FORGE_INSTANTIATE_PAIR(IT, OP, ST, NPAIR)                                              \
+    template cudaError_t forge::launch_wgrad_pair<IT, OP, ST, NPAIR>(                          \
+        const CUtensorMap&, const CUtensorMap&, const forge::Params&, int64_t, cudaStream_t);
 
 #define FORGE_DEFINE_LAUNCH()                                                                  \
     namespace forge {                                                                          \
