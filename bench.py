@@ -52,14 +52,29 @@ def load_peaks():
         return dict(PEAKS_FALLBACK), "fallback"
 
 
+def csrc_digest():
+    """sha256 over the CUDA sources (file name + content, sorted by name)."""
+    import hashlib
+    d = os.path.join(ROOT, "weight_grad_gemm_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(f.encode())
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()
+
+
 def profile_summary():
-    """Per-launch DRAM traffic of the fused kernel from the committed ncu summary."""
+    """Per-launch DRAM traffic of the fused kernel from the committed ncu
+    summary, or None when the kernel sources changed since that capture."""
     p = os.path.join(ROOT, "profiles", "fused_adamw_mlp_down.json")
     try:
         with open(p) as f:
-            return json.load(f)
+            doc = json.load(f)
     except OSError:
         return None
+    return doc if doc.get("csrc_sha256") == csrc_digest() else None
 
 
 # ---------------------------------------------------------------- clocks
