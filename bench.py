@@ -139,16 +139,21 @@ class Dense:
         self.X = wl.activations(K, N, wl.seed_of(wk.name, "X"), device=dev)
         self.D = wl.activations(K, M, wl.seed_of(wk.name, "dY"), device=dev)
         self.W = wl.randn((N, M), wl.seed_of(wk.name, "W"), device=dev, std=0.02)
-        self.m = wl.randn((N, M), wl.seed_of(wk.name, "m"), device=dev, std=1e-3).to(state_dtype)
-        self.v = (wl.randn((N, M), wl.seed_of(wk.name, "v"), device=dev, std=1e-3) ** 2).to(
-            state_dtype)
+        self.m = torch.zeros((N, M), dtype=state_dtype, device=dev)
+        self.v = torch.zeros((N, M), dtype=state_dtype, device=dev)
         self.hp = wk.adam.f32()
-        self.t = wk.first_step
+        # the state is warmed by the steps before the timed one (t = first_step)
+        self.t = 1
+        while self.t < wk.first_step:
+            self.step()
         self.flops = wk.flops
         self.params = N * M
         es = 4 if state_dtype == torch.float32 else 2
         # algorithmic bytes: X and dY read once, W read+write, m and v read+write
         self.bytes = (K * N + K * M) * 2 + N * M * (8 + 4 * es)
+
+    peak_key = "bf16"
+    opt = "AdamW"
 
     def step(self, X=None, D=None, stream=None):
         import weight_grad_gemm_gb300 as fg
@@ -157,6 +162,150 @@ class Dense:
                              self.m, self.v, lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps,
                              wd=hp.wd, step=self.t, stream=stream)
         self.t += 1
+
+    def inputs(self):
+        return [self.X, self.D]
+
+    def step_with(self, ins, stream=None):
+        self.step(ins[0], ins[1], stream=stream)
+
+    def result(self):
+        return self.W
+
+
+class AttnSet:
+    """The four attention projections of one layer (d_in 4096, d_out 4096,
+    1024, 1024, 4100; K = 16384) as four fused calls per step; d_out = 4100
+    has 8200-byte dY rows and goes through the cp.async loader."""
+
+    peak_key = "bf16"
+    opt = "AdamW"
+
+    def __init__(self, dev, state_dtype=torch.float32):
+        self.parts = [Dense(wk, dev, state_dtype) for wk in wl.ATTN_PROJ]
+        shared = self.parts[0].X
+        for p in self.parts[1:]:
+            p.X = shared  # one activation tensor feeds all four projections
+        self.wk = wl.Workload("attn_proj K=16384 d_in=4096 d_out={4096,1024,1024,4100}",
+                              K=16384, N=4096, M=sum(wl.ATTN_OUTS))
+        self.flops = sum(p.flops for p in self.parts)
+        self.params = sum(p.params for p in self.parts)
+        self.bytes = sum(p.bytes for p in self.parts)
+
+    def step(self, stream=None):
+        for p in self.parts:
+            p.step(stream=stream)
+
+    def inputs(self):
+        return [self.parts[0].X] + [p.D for p in self.parts]
+
+    def step_with(self, ins, stream=None):
+        for i, p in enumerate(self.parts):
+            p.step(ins[0], ins[1 + i], stream=stream)
+
+    def result(self):
+        return self.parts[0].W
+
+
+class MoE:
+    """Grouped call over 8 experts [14336, 4096]; the step cycles through the
+    six seeded top-2 Zipf(1.2) routings (four empty experts on even steps)."""
+
+    peak_key = "bf16"
+    opt = "AdamW"
+
+    def __init__(self, dev, state_dtype=torch.float32):
+        wk = wl.MOE
+        self.wk = wk
+        E, N, M = wk.experts, wk.N, wk.M
+        offs = []
+        for t in range(1, wk.steps + 1):
+            zero = wl.moe_zero_experts(wl.seed_of(wk.name, "zero", t), E) if t % 2 == 0 else ()
+            c = wl.zipf_top2_counts(wl.seed_of(wk.name, "route", t), tokens=16384, experts=E,
+                                    zero_experts=zero)
+            offs.append(torch.from_numpy(wl.offsets_from_counts(c).astype(np.int32)).to(dev))
+        self.offs = offs
+        T = int(offs[0][-1])
+        self.X = wl.activations(T, N, wl.seed_of(wk.name, "X"), device=dev)
+        self.D = wl.activations(T, M, wl.seed_of(wk.name, "dY"), device=dev)
+        self.W = wl.randn((E, N, M), wl.seed_of(wk.name, "W"), device=dev, std=0.02)
+        self.m = wl.randn((E, N, M), wl.seed_of(wk.name, "m"), device=dev, std=1e-3).to(state_dtype)
+        self.v = (wl.randn((E, N, M), wl.seed_of(wk.name, "v"), device=dev, std=1e-3) ** 2).to(
+            state_dtype)
+        self.hp = wk.adam.f32()
+        self.t = 1
+        self.flops = 2.0 * N * M * T
+        self.params = E * N * M
+        es = 4 if state_dtype == torch.float32 else 2
+        self.bytes = 2 * (T * N + T * M) + E * N * M * (8 + 4 * es)
+
+    def step(self, stream=None, X=None, D=None):
+        import weight_grad_gemm_gb300 as fg
+        hp = self.hp
+        off = self.offs[(self.t - 1) % len(self.offs)]
+        fg.forge_grouped_wgrad_adamw(self.X if X is None else X, self.D if D is None else D,
+                                     self.W, self.m, self.v, off, lr=hp.lr, beta1=hp.beta1,
+                                     beta2=hp.beta2, eps=hp.eps, wd=hp.wd, step=self.t,
+                                     stream=stream)
+        self.t += 1
+
+    def inputs(self):
+        return [self.X, self.D]
+
+    def step_with(self, ins, stream=None):
+        self.step(stream=stream, X=ins[0], D=ins[1])
+
+    def result(self):
+        return self.W
+
+
+class Fp8:
+    """X, dY [32768, 8192] e4m3 with per-tensor scales; AdamW or SGD momentum."""
+
+    peak_key = "fp8"
+
+    def __init__(self, dev, state_dtype=torch.float32, opt="AdamW"):
+        wk = wl.FP8
+        self.wk = wk
+        K, N, M = wk.K, wk.N, wk.M
+        self.X, sx = wl.quantize_e4m3(wl.with_outliers((K, N), wl.seed_of(wk.name, "X"), dev))
+        self.D, sy = wl.quantize_e4m3(wl.with_outliers((K, M), wl.seed_of(wk.name, "dY"), dev))
+        self.scales = torch.tensor([sx, sy], dtype=torch.float32, device=dev)
+        self.W = wl.randn((N, M), wl.seed_of(wk.name, "W"), device=dev, std=0.02)
+        self.m = wl.randn((N, M), wl.seed_of(wk.name, "m"), device=dev, std=1e-3).to(state_dtype)
+        self.v = (wl.randn((N, M), wl.seed_of(wk.name, "v"), device=dev, std=1e-3) ** 2).to(
+            state_dtype)
+        self.opt = opt
+        self.hp = wk.adam.f32() if opt == "AdamW" else wl.FP8_SGD.f32()
+        self.t = 1
+        self.flops = wk.flops
+        self.params = N * M
+        es = 4 if state_dtype == torch.float32 else 2
+        nst = 2 if opt == "AdamW" else 1
+        self.bytes = (K * N + K * M) + N * M * (8 + 2 * nst * es)
+
+    def step(self, stream=None, X=None, D=None):
+        import weight_grad_gemm_gb300 as fg
+        hp = self.hp
+        X = self.X if X is None else X
+        D = self.D if D is None else D
+        if self.opt == "AdamW":
+            fg.forge_wgrad_adamw(X, D, self.W, self.m, self.v, lr=hp.lr, beta1=hp.beta1,
+                                 beta2=hp.beta2, eps=hp.eps, wd=hp.wd, step=self.t,
+                                 scales=self.scales, stream=stream)
+        else:
+            fg.forge_wgrad_sgdm(X, D, self.W, self.m, lr=hp.lr, momentum=hp.momentum, wd=hp.wd,
+                                scales=self.scales, stream=stream)
+        self.t += 1
+
+    def inputs(self):
+        return [self.X, self.D]
+
+    def step_with(self, ins, stream=None):
+        self.step(stream=stream, X=ins[0], D=ins[1])
+
+    def result(self):
+        return self.W
 
 
 class Unfused:
@@ -186,11 +335,23 @@ class Unfused:
         self.W.grad = g.float()
         self.opt.step()
 
+    def inputs(self):
+        return [self.X, self.D]
+
+    def step_with(self, ins, stream=None):
+        self.step(ins[0], ins[1], stream=stream)
+
+    def result(self):
+        return self.W
+
 
 WORKLOADS = {
     "mlp_down": lambda dev, st: Dense(wl.MLP_DOWN, dev, st),
-    "attn_proj": lambda dev, st: Dense(wl.ATTN_PROJ[0], dev, st),
+    "attn_proj": lambda dev, st: AttnSet(dev, st),
     "linear": lambda dev, st: Dense(wl.LINEAR, dev, st),
+    "moe": lambda dev, st: MoE(dev, st),
+    "fp8": lambda dev, st: Fp8(dev, st, "AdamW"),
+    "fp8_sgdm": lambda dev, st: Fp8(dev, st, "SGD"),
 }
 
 
@@ -325,6 +486,8 @@ def main():
 
     job = WORKLOADS[args.workload](dev, torch.float32 if args.state == "f32" else torch.bfloat16)
     if args.impl == "unfused":
+        if not isinstance(job, Dense):
+            ap.error("--impl unfused is defined for the dense workloads")
         job = Unfused(job)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -366,12 +529,13 @@ def main():
     ms = total_ms / args.steps
     value = job.flops * world / (ms * 1e-3) / 1e12
 
-    # end to end through the C ABI with pinned host buffers
-    Xh = job.X.cpu().pin_memory()
-    Dh = job.D.cpu().pin_memory()
-    Wh = torch.empty(job.W.shape, dtype=job.W.dtype).pin_memory()
-    Xd = torch.empty_like(job.X)
-    Dd = torch.empty_like(job.D)
+    # end to end through the C ABI with pinned host buffers: this step's
+    # inputs are copied in and the updated parameters copied out, every step
+    ins = job.inputs()
+    ins_h = [t.cpu().pin_memory() for t in ins]
+    ins_d = [torch.empty_like(t) for t in ins]
+    res = job.result()
+    res_h = torch.empty(res.shape, dtype=res.dtype).pin_memory()
     e2e_times = []
     for i in range(args.e2e_steps + 2):
         flush.zero_()
@@ -379,11 +543,11 @@ def main():
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        Xd.copy_(Xh, non_blocking=True)
-        Dd.copy_(Dh, non_blocking=True)
-        job.step(Xd, Dd, stream=stream)
+        for d, h in zip(ins_d, ins_h):
+            d.copy_(h, non_blocking=True)
+        job.step_with(ins_d, stream=stream)
         with torch.no_grad():
-            Wh.copy_(job.W, non_blocking=True)
+            res_h.copy_(job.result(), non_blocking=True)
         b.record(stream)
         b.synchronize()
         if i >= 2:
@@ -394,16 +558,22 @@ def main():
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
-    h2d = (Xh.numel() + Dh.numel()) * 2
-    d2h = Wh.numel() * 4
+    h2d = sum(h.numel() * h.element_size() for h in ins_h)
+    d2h = res_h.numel() * res_h.element_size()
 
     peaks, peak_src = load_peaks()
     peak_tf = peaks["bf16_tflops"]
+    peak_note = f"bf16_tflops burst, {peak_src}"
+    if getattr(job, "peak_key", "bf16") == "fp8":
+        # e4m3 dense rate = the measured bf16 rate x the nominal fp8 / bf16 ratio (4.5 / 2.25)
+        peak_tf = peaks["bf16_tflops"] * 2.0
+        peak_note = f"bf16_tflops burst x 2 (nominal fp8/bf16), {peak_src}"
     bw = peaks["hbm_gbs"]
     kernel_tf = job.flops / (ms * 1e-3) / 1e12
     t_tensor = job.flops / (peak_tf * 1e12)
     t_hbm = job.bytes / (bw * 1e9)
-    prof = profile_summary()
+    prof = profile_summary() if (args.workload == "mlp_down" and args.state == "f32" and
+                                 args.impl == "ours") else None
     traffic = prof.get("dram_bytes_per_launch") if prof else None
     gradw = prof.get("grad_w_hbm_bytes") if prof else None
 
@@ -412,7 +582,7 @@ def main():
         "impl": args.impl,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": job.wk.name + f" AdamW {args.state} state",
+        "config": {"workload": job.wk.name + f" {getattr(job, 'opt', 'AdamW')} {args.state} state",
                    "K": job.wk.K, "d_in": job.wk.N, "d_out": job.wk.M,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between steps (512 MiB write); inputs+state 1.0 GB > L2"},
@@ -421,14 +591,15 @@ def main():
         "grad_w_hbm_bytes": gradw,
         "roofline": {"bound": "tensor" if t_tensor >= t_hbm else "hbm", "achieved": kernel_tf,
                      "peak": peak_tf, "unit": "TFLOP/s", "frac": kernel_tf / peak_tf,
-                     "peak_source": f"bf16_tflops burst, {peak_src}", "traffic": traffic},
+                     "peak_source": peak_note, "traffic": traffic},
         "e2e": {"value": job.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps if args.impl == "ours" else 0,
+        "gpu_launches": args.steps * len(getattr(job, "parts", [None])) if args.impl == "ours" else 0,
         "clocks": clk,
         "wall_s_timed_region": wall,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.impl == "ours":
+    if (rank == 0 and world == 1 and not args.no_cpu_baseline and args.impl == "ours" and
+            isinstance(job, Dense)):
         line["cpu_baseline"] = cpu_baseline(job)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -56,7 +56,10 @@ def _band(exact):
     return STATE_DIAG_RMS * rms(exact) + STATE_DIAG_REL * np.abs(exact)
 
 
-def check_state_f32(gpu, exact, name="state"):
+def check_state_f32(gpu, exact, name="state", diag=True):
+    """Contract bound always; the tight diagnostic band when `diag` (it is
+    calibrated for K up to about a thousand tokens, where fp32 accumulation
+    error in g stays below it)."""
     gpu = np.asarray(gpu, np.float64)
     exact = np.asarray(exact, np.float64)
     if not gpu.size:
@@ -64,20 +67,24 @@ def check_state_f32(gpu, exact, name="state"):
     bound = STATE_TOL * rms(exact)
     err = np.abs(gpu - exact)
     assert err.max() <= bound, f"{name}: max |error| {err.max():.3e} > 2e-3*rms = {bound:.3e}"
-    over = err > _band(exact)
-    assert not over.any(), (f"{name}: {int(over.sum())} elements beyond the diagnostic band "
-                            f"(worst {err.max():.3e}, rms {rms(exact):.3e})")
+    if diag:
+        over = err > _band(exact)
+        assert not over.any(), (f"{name}: {int(over.sum())} elements beyond the diagnostic band "
+                                f"(worst {err.max():.3e}, rms {rms(exact):.3e})")
     return float(err.max())
 
 
-def check_state_bf16(gpu_bits, exact, name="state"):
+def check_state_bf16(gpu_bits, exact, name="state", diag=True):
+    """The stored bf16 must be the rounding of some value within the band of
+    the exact value: the diagnostic band when `diag`, else the contract's
+    2e-3 * rms."""
     gpu_bits = np.asarray(gpu_bits).astype(np.uint16).ravel()
     exact = np.asarray(exact, np.float64).ravel()
     rn = oracle.round_bf16(exact)
     bad = np.nonzero(gpu_bits != rn)[0]
     if bad.size == 0:
         return 0
-    band = _band(exact)[bad]
+    band = (_band(exact) if diag else np.full(exact.shape, STATE_TOL * rms(exact)))[bad]
     x = exact[bad]
     g = oracle.decode(gpu_bits[bad])
     lo = oracle.decode(oracle.round_bf16(x - band))
@@ -103,3 +110,16 @@ def check_W(gpu_W, exact_W, G, lr, m_exact=None, name="W"):
     err = np.max(np.abs(gpu_W - exact_W)[mask]) if mask.any() else 0.0
     assert err <= W_TOL * lr, f"{name}: max |error| {err:.3e} > 1e-2*lr = {W_TOL * lr:.3e}"
     return err
+
+
+def check_grad_from_m(m_gpu, m_old, G, beta1, name="g from m"):
+    """Reconstruct the gradient the kernel used from m' = b1 m + (1-b1) g and
+    compare it with the oracle's g: the dW contract (relative Frobenius
+    <= 2e-3) and a diagnostic bound of 1e-4 for long contractions."""
+    m_gpu = np.asarray(m_gpu, np.float64)
+    m_old = np.asarray(m_old, np.float64)
+    g = (m_gpu - beta1 * m_old) / (1.0 - beta1)
+    e = rel_fro(g, G)
+    assert e <= DW_TOL["bf16"], f"{name}: relative Frobenius {e:.3e} > {DW_TOL['bf16']}"
+    assert e <= 1e-4, f"{name}: relative Frobenius {e:.3e} > diagnostic 1e-4"
+    return e
