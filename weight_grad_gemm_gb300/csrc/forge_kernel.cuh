@@ -460,39 +460,52 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, 
 constexpr int kLoaderWarp0 = 2;  // warps 2 and 3
 constexpr int kLoaderThreads = 64;
 
-// Copies one operand's k-block [k0, k0 + BK) x [mn0, mn0 + tile_mn) into the
+// Copies one operand's k-block [k0, k0 + BK) x [mn0, mn0 + TILE_MN) into the
 // same 128-byte-swizzled layout TMA would produce: column block `box` (128
 // bytes of the contiguous dimension) at box * box_bytes, k row r at r * 128,
 // 16-byte chunk c of the row at (c ^ (r & 7)) * 16.  Rows at or past k_lim
-// and columns at or past mn_lim are zero-filled.
-template <int IT>
+// and columns at or past mn_lim are zero-filled.  GRAN is the copy width in
+// bytes (8 or 4); every division below is by a compile-time constant.
+template <int IT, int TILE_MN, int GRAN>
 __device__ __forceinline__ void load_block_cp_async(uint8_t* stage, const uint8_t* g, int64_t ld,
                                                     int64_t mn0, int64_t mn_lim, int64_t k0,
-                                                    int64_t k_lim, int tile_mn, int gran, int tid)
+                                                    int64_t k_lim, int tid)
 {
     using TR = InTraits<IT>;
     constexpr int BK = TR::BK;
     constexpr int es = TR::esize;
     constexpr int box_bytes = TR::box_mn * es * BK;
-    const int units_per_row = tile_mn * es / gran;
-    const int total = BK * units_per_row;
-    for (int u = tid; u < total; u += kLoaderThreads) {
-        const int r = u / units_per_row;
-        const int cb = (u - r * units_per_row) * gran;  // byte offset in the tile row
-        const int box = cb >> 7;
-        const int inb = cb & 127;
-        uint8_t* d = stage + box * box_bytes + r * 128 + (((inb >> 4) ^ (r & 7)) << 4) + (inb & 15);
+    constexpr int kUnitsPerRow = TILE_MN * es / GRAN;
+    constexpr int kTotal = BK * kUnitsPerRow;
+    static_assert(kTotal % kLoaderThreads == 0, "whole passes");
+#pragma unroll 4
+    for (int u = tid; u < kTotal; u += kLoaderThreads) {
+        const int r = u / kUnitsPerRow;
+        const int cb = (u - r * kUnitsPerRow) * GRAN;  // byte offset in the tile row
+        uint8_t* d = stage + (cb >> 7) * box_bytes + r * 128 +
+                     ((((cb & 127) >> 4) ^ (r & 7)) << 4) + (cb & 15);
         const int64_t k = k0 + r;
         const int64_t col = mn0 + cb / es;
         int src_bytes = 0;
         const uint8_t* src = g;
         if (k < k_lim && col < mn_lim) {
             const int64_t avail = (mn_lim - col) * es;
-            src_bytes = avail >= gran ? gran : static_cast<int>(avail);
+            src_bytes = avail >= GRAN ? GRAN : static_cast<int>(avail);
             src = g + (k * ld + col) * es;
         }
-        ptx::cp_async(d, src, gran, src_bytes);
+        ptx::cp_async(d, src, GRAN, src_bytes);
     }
+}
+
+template <int IT, int TILE_MN>
+__device__ __forceinline__ void load_block_cp_async(uint8_t* stage, const uint8_t* g, int64_t ld,
+                                                    int64_t mn0, int64_t mn_lim, int64_t k0,
+                                                    int64_t k_lim, int gran, int tid)
+{
+    if (gran == 8)
+        load_block_cp_async<IT, TILE_MN, 8>(stage, g, ld, mn0, mn_lim, k0, k_lim, tid);
+    else
+        load_block_cp_async<IT, TILE_MN, 4>(stage, g, ld, mn0, mn_lim, k0, k_lim, tid);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -746,33 +759,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (MANUAL && (warp == kLoaderWarp0 || warp == kLoaderWarp0 + 1)) {
         // ---------------------------------------------------- cp.async loader
-        // Fills the operands TMA cannot address, one stage behind its own
-        // issue: after issuing stage s it waits for the copies of the
-        // previous stage, makes them visible to the tensor core (proxy
-        // fence) and arrives on that stage's full barrier.
+        // Fills the operands TMA cannot address.  Each thread keeps up to
+        // kLag stages of its copies in flight; a stage is announced (proxy
+        // fence, then an arrive on its full barrier) once its copies are
+        // complete: when more than kLag are outstanding, and all of them
+        // whenever the next slot is not free yet, so no announcement waits
+        // on the MMA.
+        constexpr int kLag = kStages - 1;
         const int tid = threadIdx.x - kLoaderWarp0 * 32;
         int s = 0;
         uint32_t ph = 0;
-        int prev = -1;
+        int npend = 0;  // stages issued but not yet announced, oldest first
         bool ok = true;
         for (int32_t t = sc.first; ok && t < sc.total; t += sc.step) {
             const Tile tl = sc.get(t);
             for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
+                // Announce every pending stage before blocking on a busy slot.
+                if (npend > 0 && !ptx::mbar_test_wait(ptx::smem_addr(&empty[s]), ph ^ 1u)) {
+                    ptx::cp_async_wait<0>();
+                    ptx::fence_proxy_async_smem();
+                    for (; npend > 0; --npend)
+                        ptx::mbar_arrive(&full[(s - npend + kStages) % kStages]);
+                }
                 ok = warp_wait(&empty[s], ph ^ 1u, abort_flag, p, lane);
                 if (!ok) break;
                 uint8_t* sa = smem + s * kStageBytes;
                 if (p.manual_a)
-                    load_block_cp_async<IT>(sa, p.gA, p.M, tl.m0, p.M, k, tl.k_end, BM, p.gran_a, tid);
+                    load_block_cp_async<IT, BM>(sa, p.gA, p.M, tl.m0, p.M, k, tl.k_end, p.gran_a,
+                                                tid);
                 if (p.manual_b)
-                    load_block_cp_async<IT>(sa + kStageA, p.gB, p.N, tl.n0, p.N, k, tl.k_end, BN,
-                                            p.gran_b, tid);
+                    load_block_cp_async<IT, BN>(sa + kStageA, p.gB, p.N, tl.n0, p.N, k, tl.k_end,
+                                                p.gran_b, tid);
                 ptx::cp_async_commit();
-                if (prev >= 0) {
-                    ptx::cp_async_wait<1>();
+                if (++npend > kLag) {
+                    ptx::cp_async_wait<kLag>();
                     ptx::fence_proxy_async_smem();
-                    ptx::mbar_arrive(&full[prev]);
+                    ptx::mbar_arrive(&full[(s - kLag + kStages) % kStages]);
+                    --npend;
                 }
-                prev = s;
                 if (++s == kStages) {
                     s = 0;
                     ph ^= 1u;
@@ -780,9 +804,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         ptx::cp_async_wait<0>();
-        if (prev >= 0 && ok) {
+        if (ok) {
             ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(&full[prev]);
+            for (; npend > 0; --npend) ptx::mbar_arrive(&full[(s - npend + kStages) % kStages]);
         }
     } else if (warp >= kEpiWarp0) {
         epilogue_role<IT, OP, ST>(p, sc, smem, tfull, tmem_base, abort_flag, warp, lane,
