@@ -126,8 +126,29 @@ struct Sched {
     int32_t tiles_m, tiles_n, per_expert, total;
     int32_t m_step;        // d_out rows per tile: 128 (one CTA) or 256 (CTA pair)
     int32_t m_off;         // this CTA's first row within the tile (128 for the odd CTA of a pair)
-    int32_t first, step;   // this CTA's walk over the tile list: first, first + step, ...
+    int32_t first, step;   // this CTA's share of the tile list: first, first + step, ...
+    int32_t count;         // tiles in this CTA's share
+    int32_t alternate;     // walk the share front, back, front, ... (grouped)
     int32_t band;          // d_out tiles per raster band (tiles_m: plain m-fastest order)
+
+    // The i-th tile this CTA processes.  With `alternate`, a share of the
+    // heavy-first grouped list is walked from both ends, so heavy tiles
+    // (MMA-bound) and light ones (epilogue-bound, down to decay-only tiles of
+    // experts without tokens) alternate and overlap through the two
+    // accumulators.
+    __device__ __forceinline__ int32_t nth(int32_t i) const
+    {
+        const int32_t j = alternate ? ((i & 1) ? count - 1 - (i >> 1) : (i >> 1)) : i;
+        return first + j * step;
+    }
+
+    __device__ __forceinline__ void set_share(int32_t f, int32_t s, int32_t alt)
+    {
+        first = f;
+        step = s;
+        count = f < total ? (total - f + s - 1) / s : 0;
+        alternate = alt;
+    }
     const int32_t* offs;   // smem copy of offsets (grouped) or null
     const int32_t* order;  // smem expert order (grouped) or null
     int64_t K, MN;
@@ -326,7 +347,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, 
     float gscale = 1.0f;
     if constexpr (IT == IN_E4M3) gscale = p.scales[0] * p.scales[1];
     uint32_t ct = 0;
-    for (int32_t t = sc.first; t < sc.total; t += sc.step) {
+    for (int32_t it = 0; it < sc.count; ++it) {
+        const int32_t t = sc.nth(it);
         const Tile tl = sc.get(t);
         const bool has_acc = tl.k_end > tl.k_begin;
         const uint32_t b = ct & 1u;
@@ -603,11 +625,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     sc.tiles_n = p.tiles_n;
     sc.m_step = BM;
     sc.m_off = 0;
-    sc.first = blockIdx.x;
-    sc.step = gridDim.x;
     sc.band = p.raster_band;
     sc.per_expert = p.tiles_m * p.tiles_n;
     sc.total = sc.per_expert * p.E;
+    sc.set_share(blockIdx.x, gridDim.x, GROUPED ? 1 : 0);
     sc.offs = GROUPED ? s_offs : nullptr;
     sc.order = GROUPED ? s_order : nullptr;
     sc.K = p.K;
@@ -626,7 +647,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             uint32_t issued_mask = 0, last_parity = 0;
             bool ok = true;
-            for (int32_t t = sc.first; ok && t < sc.total; t += sc.step) {
+            for (int32_t it = 0; ok && it < sc.count; ++it) {
+                const int32_t t = sc.nth(it);
                 const Tile tl = sc.get(t);
                 for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
                     if (!wait_bounded(&empty[s], ph ^ 1u, abort_flag, p)) {
@@ -679,7 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ct = 0;  // accumulator tiles issued by this CTA
         bool ok = true;
         bool issued_any = false;
-        for (int32_t t = sc.first; ok && t < sc.total; t += sc.step) {
+        for (int32_t it = 0; ok && it < sc.count; ++it) {
+                const int32_t t = sc.nth(it);
             const Tile tl = sc.get(t);
             if (tl.k_end <= tl.k_begin) continue;  // no tokens: epilogue-only tile
             const uint32_t b = ct & 1u;
@@ -771,7 +794,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ph = 0;
         int npend = 0;  // stages issued but not yet announced, oldest first
         bool ok = true;
-        for (int32_t t = sc.first; ok && t < sc.total; t += sc.step) {
+        for (int32_t it = 0; ok && it < sc.count; ++it) {
+                const int32_t t = sc.nth(it);
             const Tile tl = sc.get(t);
             for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
                 // Announce every pending stage before blocking on a busy slot.
@@ -924,11 +948,10 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
     sc.tiles_n = p.tiles_n;
     sc.m_step = 2 * NPAIR * BM;
     sc.m_off = static_cast<int32_t>(crank) * BM;
-    sc.first = blockIdx.x / (2 * NPAIR);
-    sc.step = gridDim.x / (2 * NPAIR);
     sc.band = p.raster_band;
     sc.per_expert = p.tiles_m * p.tiles_n;
     sc.total = sc.per_expert;
+    sc.set_share(blockIdx.x / (2 * NPAIR), gridDim.x / (2 * NPAIR), 0);
     sc.offs = nullptr;
     sc.order = nullptr;
     sc.K = p.K;
@@ -944,7 +967,8 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             uint32_t issued_mask = 0, last_parity = 0;
             bool ok = true;
-            for (int32_t t = sc.first; ok && t < sc.total; t += sc.step) {
+            for (int32_t it = 0; ok && it < sc.count; ++it) {
+                const int32_t t = sc.nth(it);
                 const Tile tl = sc.get(t);
                 for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
                     if (!wait_bounded(&empty[s], ph ^ 1u, abort_flag, p)) {
@@ -1001,7 +1025,8 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t ct = 0;
             bool ok = true;
             bool issued_any = false;
-            for (int32_t t = sc.first; ok && t < sc.total; t += sc.step) {
+            for (int32_t it = 0; ok && it < sc.count; ++it) {
+                const int32_t t = sc.nth(it);
                 const Tile tl = sc.get(t);
                 if (tl.k_end <= tl.k_begin) continue;
                 const uint32_t b = ct & 1u;
