@@ -153,6 +153,12 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t 
                  : "memory");
 }
 
+// Prefetch the 128-byte line holding `p` into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the
 // async proxy (TMA, tensor core) before a later async operation reads them.
 __device__ __forceinline__ void fence_proxy_async_smem()
