@@ -16,8 +16,8 @@
 //
 // Roles (384 threads, one CTA per SM, persistent over a static tile list):
 //   warp 0      TMA producer: K-blocks of dY and X into a 4-stage ring
-//   warp 1      TMEM allocator; lane 0 issues tcgen05.mma into one of two
-//               128x256 fp32 accumulators (512 TMEM columns)
+//   warp 1      TMEM allocator; lane 0 alone issues tcgen05.mma into one of
+//               two 128x256 fp32 accumulators (512 TMEM columns)
 //   warps 4-11  epilogue: tcgen05.ld the accumulator, apply AdamW / SGD-m /
 //               plain store, write W and the state back; two warpgroups
 //               split the 256 columns
@@ -694,53 +694,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- UMMA issuer
-        // The whole warp walks the schedule; lane 0 waits on the barriers
-        // and issues the MMAs, all lanes take part in clearing rows.
-        int s = 0;
-        uint32_t ph = 0;
-        uint32_t ct = 0;  // accumulator tiles issued by this CTA
-        bool ok = true;
-        bool issued_any = false;
-        for (int32_t it = 0; ok && it < sc.count; ++it) {
+        // Lane 0 alone waits on the barriers and issues the MMAs: a
+        // warp-wide loop would add a warp synchronisation to every stage and
+        // keep the issuer from running ahead of the tensor pipe.
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t ct = 0;  // accumulator tiles issued by this CTA
+            bool ok = true;
+            bool issued_any = false;
+            for (int32_t it = 0; ok && it < sc.count; ++it) {
                 const int32_t t = sc.nth(it);
-            const Tile tl = sc.get(t);
-            if (tl.k_end <= tl.k_begin) continue;  // no tokens: epilogue-only tile
-            const uint32_t b = ct & 1u;
-            const uint32_t aph = (ct >> 1) & 1u;
-            ok = warp_wait(&tempty[b], aph ^ 1u, abort_flag, p, lane);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            const uint32_t d_tmem = tmem_base + b * BN;
-            uint32_t first = 1;
-            for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
-                ok = warp_wait(&full[s], ph, abort_flag, p, lane);
+                const Tile tl = sc.get(t);
+                if (tl.k_end <= tl.k_begin) continue;  // no tokens: epilogue-only tile
+                const uint32_t b = ct & 1u;
+                const uint32_t aph = (ct >> 1) & 1u;
+                ok = wait_bounded(&tempty[b], aph ^ 1u, abort_flag, p);
                 if (!ok) break;
                 ptx::tc_fence_after();
-                if constexpr (GROUPED) {
-                    // Rows past this expert's last token belong to the next
-                    // expert (TMA zero-fills only outside the tensor), so they
-                    // are cleared in the A operand before the tensor core
-                    // reads the stage.  With MN-major 128-byte swizzle each k
-                    // row is one whole 128-byte line per column block, so a
-                    // row is cleared without undoing the swizzle.
-                    const int64_t valid = tl.k_end - k;
-                    if (valid < BK) {
-                        const int rows = BK - static_cast<int>(valid);
-                        const int units = rows * kABoxes * 8;  // 16-byte units
-                        for (int u = lane; u < units; u += 32) {
-                            const int c = u & 7;
-                            const int rb = u >> 3;
-                            const int i = rb % kABoxes;
-                            const int r = static_cast<int>(valid) + rb / kABoxes;
-                            uint4* row = reinterpret_cast<uint4*>(smem + s * kStageBytes +
-                                                                  i * kBoxBytes + r * 128);
-                            row[c] = make_uint4(0, 0, 0, 0);
+                const uint32_t d_tmem = tmem_base + b * BN;
+                uint32_t first = 1;
+                for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
+                    ok = wait_bounded(&full[s], ph, abort_flag, p);
+                    if (!ok) break;
+                    if constexpr (GROUPED) {
+                        // Rows past this expert's last token belong to the next
+                        // expert (TMA zero-fills only outside the tensor), so
+                        // they are cleared in the A operand before the tensor
+                        // core reads the stage.  With MN-major 128-byte swizzle
+                        // each k row is one whole 128-byte line per column
+                        // block, so a row is cleared without undoing the swizzle.
+                        const int64_t valid = tl.k_end - k;
+                        if (valid < BK) {
+                            ptx::fence_proxy_async_smem();  // after the TMA writes
+                            for (int r = static_cast<int>(valid); r < BK; ++r)
+#pragma unroll
+                                for (int i = 0; i < kABoxes; ++i) {
+                                    uint4* row = reinterpret_cast<uint4*>(
+                                        smem + s * kStageBytes + i * kBoxBytes + r * 128);
+#pragma unroll
+                                    for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+                                }
+                            ptx::fence_proxy_async_smem();  // before the tensor core reads
                         }
-                        ptx::fence_proxy_async_smem();
-                        __syncwarp();
                     }
-                }
-                if (lane == 0) {
                     const uint32_t sa = ptx::smem_addr(smem + s * kStageBytes);
                     const uint32_t sb = sa + kStageA;
 #pragma unroll
@@ -756,30 +753,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         first = 0;
                     }
                     ptx::umma_commit(&empty[s]);  // stage free once these MMAs are done
+                    issued_any = true;
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
-                __syncwarp();
-                first = 0;
-                issued_any = true;
-                if (++s == kStages) {
-                    s = 0;
-                    ph ^= 1u;
+                if (!ok) break;
+                ptx::umma_commit(&tfull[b]);  // accumulator ready
+                ++ct;
+            }
+            if (!ok && issued_any) {
+                // Wait (bounded) until every MMA this thread issued is done.
+                ptx::umma_commit(drain);
+                const uint32_t a = ptx::smem_addr(drain);
+                const uint64_t t0 = ptx::globaltimer_ns();
+                while (!ptx::mbar_try_wait(a, 0)) {
+                    if (static_cast<int64_t>(ptx::globaltimer_ns() - t0) > p.timeout_ns) break;
                 }
             }
-            if (!ok) break;
-            if (lane == 0) ptx::umma_commit(&tfull[b]);  // accumulator ready
-            __syncwarp();
-            ++ct;
         }
-        if (!ok && issued_any && lane == 0) {
-            // Wait (bounded) until every MMA this thread issued is done.
-            ptx::umma_commit(drain);
-            const uint32_t a = ptx::smem_addr(drain);
-            const uint64_t t0 = ptx::globaltimer_ns();
-            while (!ptx::mbar_try_wait(a, 0)) {
-                if (static_cast<int64_t>(ptx::globaltimer_ns() - t0) > p.timeout_ns) break;
-            }
-        }
-        __syncwarp();
     } else if (MANUAL && (warp == kLoaderWarp0 || warp == kLoaderWarp0 + 1)) {
         // ---------------------------------------------------- cp.async loader
         // Fills the operands TMA cannot address.  Each thread keeps up to
@@ -1019,7 +1012,8 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- pair MMA issuer (even CTA)
-        if (leader) {
+        // Lane 0 alone waits and issues (no warp synchronisation per stage).
+        if (leader && lane == 0) {
             int s = 0;
             uint32_t ph = 0;
             uint32_t ct = 0;
@@ -1031,35 +1025,30 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
                 if (tl.k_end <= tl.k_begin) continue;
                 const uint32_t b = ct & 1u;
                 const uint32_t aph = (ct >> 1) & 1u;
-                ok = warp_wait(&tempty[b], aph ^ 1u, abort_flag, p, lane);
+                ok = wait_bounded(&tempty[b], aph ^ 1u, abort_flag, p);
                 if (!ok) break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + b * BN;
                 uint32_t first = 1;
                 for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
-                    ok = warp_wait(&full[s], ph, abort_flag, p, lane);
+                    ok = wait_bounded(&full[s], ph, abort_flag, p);
                     if (!ok) break;
-                    ptx::tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t sa = ptx::smem_addr(smem + s * kPairStageBytes);
-                        const uint32_t sb = sa + kPairStageA;
+                    const uint32_t sa = ptx::smem_addr(smem + s * kPairStageBytes);
+                    const uint32_t sb = sa + kPairStageA;
 #pragma unroll
-                        for (int ks = 0; ks < kKSteps; ++ks) {
-                            const uint64_t ad =
-                                ptx::smem_desc_sw128(sa + ks * kKStepBytes, kBoxBytes, 1024);
-                            const uint64_t bd =
-                                ptx::smem_desc_sw128(sb + ks * kKStepBytes, kBoxBytes, 1024);
-                            if constexpr (IT == IN_BF16)
-                                ptx::umma_f16_pair(d_tmem, ad, bd, kIdesc, first ? 0u : 1u);
-                            else
-                                ptx::umma_f8_pair(d_tmem, ad, bd, kIdesc, first ? 0u : 1u);
-                            first = 0;
-                        }
-                        // stage s of every CTA that received this pair's loads is free
-                        ptx::umma_commit_pair(&empty[s], kAllMask);
+                    for (int ks = 0; ks < kKSteps; ++ks) {
+                        const uint64_t ad =
+                            ptx::smem_desc_sw128(sa + ks * kKStepBytes, kBoxBytes, 1024);
+                        const uint64_t bd =
+                            ptx::smem_desc_sw128(sb + ks * kKStepBytes, kBoxBytes, 1024);
+                        if constexpr (IT == IN_BF16)
+                            ptx::umma_f16_pair(d_tmem, ad, bd, kIdesc, first ? 0u : 1u);
+                        else
+                            ptx::umma_f8_pair(d_tmem, ad, bd, kIdesc, first ? 0u : 1u);
+                        first = 0;
                     }
-                    __syncwarp();
-                    first = 0;
+                    // stage s of every CTA that received this pair's loads is free
+                    ptx::umma_commit_pair(&empty[s], kAllMask);
                     issued_any = true;
                     if (++s == kPairStages) {
                         s = 0;
@@ -1067,11 +1056,10 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                if (lane == 0) ptx::umma_commit_pair(&tfull[b], pair_mask);  // both accumulators ready
-                __syncwarp();
+                ptx::umma_commit_pair(&tfull[b], pair_mask);  // both accumulators ready
                 ++ct;
             }
-            if (!ok && issued_any && lane == 0) {
+            if (!ok && issued_any) {
                 ptx::umma_commit_pair(drain, static_cast<uint16_t>(1u << crank));
                 const uint32_t a = ptx::smem_addr(drain);
                 const uint64_t t0 = ptx::globaltimer_ns();
@@ -1079,7 +1067,6 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
                     if (static_cast<int64_t>(ptx::globaltimer_ns() - t0) > p.timeout_ns) break;
                 }
             }
-            __syncwarp();
         }
     } else if (warp >= kEpiWarp0) {
         const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), lead_rank);
