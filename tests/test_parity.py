@@ -251,8 +251,15 @@ def check_grouped(got, X, D, off, W, m, v, step, sc, state_bf16, hp=HP):
         check_adamw((got[0][e], got[1][e], got[2][e]), sub, G, hp.lr, state_bf16)
 
 
+@pytest.fixture(params=["single", "pair"])
+def grouped_form(request, monkeypatch):
+    """Run a grouped test on the one-CTA kernel and on CTA pairs."""
+    monkeypatch.setenv("FORGE_KERNEL", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("state_bf16", [False, True], ids=["f32state", "bf16state"])
-def test_grouped_ragged_with_empty_experts(cuda_device, state_bf16):
+def test_grouped_ragged_with_empty_experts(cuda_device, grouped_form, state_bf16):
     counts = [37, 0, 100, 64, 3, 0, 129]
     N, M = 264, 136
     X, D, off, W, m, v, sc = grouped_case(counts, N, M, 13, state_bf16)
@@ -260,7 +267,7 @@ def test_grouped_ragged_with_empty_experts(cuda_device, state_bf16):
     check_grouped(got, X, D, off, W, m, v, 3, sc, state_bf16)
 
 
-def test_grouped_e4m3(cuda_device):
+def test_grouped_e4m3(cuda_device, grouped_form):
     counts = [200, 0, 57, 128]
     N, M = 272, 144
     X, D, off, W, m, v, sc = grouped_case(counts, N, M, 14, kind="e4m3")
@@ -268,7 +275,7 @@ def test_grouped_e4m3(cuda_device):
     check_grouped(got, X, D, off, W, m, v, 2, sc, False)
 
 
-def test_grouped_all_experts_empty(cuda_device):
+def test_grouped_all_experts_empty(cuda_device, grouped_form):
     counts = [0, 0, 0]
     N, M = 256, 128
     X, D, off, W, m, v, sc = grouped_case(counts, N, M, 15)
@@ -280,13 +287,33 @@ def test_grouped_all_experts_empty(cuda_device):
         check_W(got[0][e], ref["W_exact"][e], np.zeros((N, M)), HP.lr, m_exact=ref["m_exact"][e])
 
 
-def test_grouped_single_expert_equals_dense_bitwise(cuda_device):
+def test_grouped_single_expert_equals_dense_bitwise(cuda_device, grouped_form):
     K, N, M = 300, 520, 296
     X, D, off, W, m, v, _ = grouped_case([K], N, M, 16)
     g = run_grouped(cuda_device, X, D, off, W, m, v, step=2)
     d = run_adamw(cuda_device, X, D, W[0], m[0], v[0], step=2)
     for a, b in zip(g, d):
         assert np.array_equal(a[0], b)
+
+
+def test_grouped_foreign_tokens_never_enter(cuda_device, grouped_form):
+    """Expert e's gradient is the sum over its own tokens only: non-finite
+    values in a neighbour's rows (which share the partial k-blocks at both
+    ends of expert 1's segment) leave experts 0 and 2 exact."""
+    counts = [40, 50, 30]
+    N, M = 264, 264
+    X, D, off, W, m, v, sc = grouped_case(counts, N, M, 23)
+    X, D = X.clone(), D.clone()
+    X[41, 5] = float("inf")
+    X[60, :] = float("nan")
+    D[45, 7] = float("-inf")
+    got = run_grouped(cuda_device, X, D, off, W, m, v, step=2)
+    ref = oracle.grouped_adamw(X, D, off, W, m, v, step=2, **vars(HP))
+    for e in (0, 2):
+        assert np.all(np.isfinite(got[0][e]))
+        G = oracle.wgrad(X, D, k_range=(int(off[e]), int(off[e + 1])))
+        sub = {k: ref[k][e] for k in ("W_exact", "m_exact", "v_exact")}
+        check_adamw((got[0][e], got[1][e], got[2][e]), sub, G, HP.lr, False)
 
 
 # ------------------------------------------------------------------ invariance (P1, no atomics)
@@ -302,7 +329,7 @@ def test_bitwise_run_to_run(cuda_device, kernel_form):
 
 
 @pytest.mark.parametrize("state_bf16", [False, True], ids=["f32state", "bf16state"])
-def test_grouped_bitwise_across_expert_segment_order(cuda_device, state_bf16):
+def test_grouped_bitwise_across_expert_segment_order(cuda_device, grouped_form, state_bf16):
     counts = [70, 0, 133, 64, 9]
     N, M = 264, 136
     X, D, off, W, m, v, _ = grouped_case(counts, N, M, 19, state_bf16)
@@ -411,7 +438,7 @@ def test_offset_base_pointers(cuda_device):
     check_dw(dW.cpu().numpy(), oracle.wgrad(X, D))
 
 
-def test_grouped_misaligned_rows(cuda_device):
+def test_grouped_misaligned_rows(cuda_device, grouped_form):
     counts = [37, 0, 100, 9]
     N, M = 264, 4100
     X, D, off, W, m, v, sc = grouped_case(counts, N, M, 46)

@@ -96,7 +96,8 @@ forge_status current_device(DeviceInfo** out)
 }
 
 // 2-D token-major operand [rows, inner] -> TMA map with 128-byte swizzled
-// boxes of (128 bytes of the inner dimension) x (k rows per stage).
+// boxes of (128 bytes of the inner dimension) x (k rows per stage / row_split).
+// row_split = 0 asks for one-row boxes, the form tile::gather4 copies use.
 forge_status encode_operand(CUtensorMap* map, const void* base, forge_dtype dt, int64_t inner,
                             int64_t rows, int row_split = 1)
 {
@@ -114,7 +115,9 @@ forge_status encode_operand(CUtensorMap* map, const void* base, forge_dtype dt, 
     const int es = elem_size(dt);
     const cuuint32_t box_inner = 128 / es;
     const cuuint32_t box_rows =
-        (dt == FORGE_BF16 ? InTraits<IN_BF16>::BK : InTraits<IN_E4M3>::BK) / row_split;
+        row_split == 0 ? 1
+                       : (dt == FORGE_BF16 ? InTraits<IN_BF16>::BK : InTraits<IN_E4M3>::BK) /
+                             row_split;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * es};
     cuuint32_t box[2] = {box_inner, box_rows};
@@ -148,56 +151,64 @@ __global__ void forge_wait_selftest_kernel(int64_t timeout_ns, int* status)
 
 forge_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FORGE_OK : FORGE_ERR_CUDA; }
 
+// The four operand maps of one call: dY and X with whole k-block boxes, and
+// (grouped calls) the same tensors with one-row boxes for gathered blocks.
+struct Maps {
+    CUtensorMap a, b, a1, b1;
+};
+
 template <int IT, bool MAN>
-cudaError_t dispatch_op(int op, int st, bool grouped, const CUtensorMap& a, const CUtensorMap& b,
-                        const Params& p, int grid, cudaStream_t s)
+cudaError_t dispatch_op(int op, int st, bool grouped, const Maps& m, const Params& p, int grid,
+                        cudaStream_t s)
 {
-    if (grouped) {
-        return st == ST_F32 ? launch_wgrad<IT, OP_ADAMW, ST_F32, true, MAN>(a, b, p, grid, s)
-                            : launch_wgrad<IT, OP_ADAMW, ST_BF16, true, MAN>(a, b, p, grid, s);
-    }
+#define FORGE_L(OPV, STV, G) launch_wgrad<IT, OPV, STV, G, MAN>(m.a, m.b, m.a1, m.b1, p, grid, s)
+    if (grouped)
+        return st == ST_F32 ? FORGE_L(OP_ADAMW, ST_F32, true) : FORGE_L(OP_ADAMW, ST_BF16, true);
     switch (op) {
     case OP_ADAMW:
-        return st == ST_F32 ? launch_wgrad<IT, OP_ADAMW, ST_F32, false, MAN>(a, b, p, grid, s)
-                            : launch_wgrad<IT, OP_ADAMW, ST_BF16, false, MAN>(a, b, p, grid, s);
+        return st == ST_F32 ? FORGE_L(OP_ADAMW, ST_F32, false) : FORGE_L(OP_ADAMW, ST_BF16, false);
     case OP_SGDM:
-        return st == ST_F32 ? launch_wgrad<IT, OP_SGDM, ST_F32, false, MAN>(a, b, p, grid, s)
-                            : launch_wgrad<IT, OP_SGDM, ST_BF16, false, MAN>(a, b, p, grid, s);
+        return st == ST_F32 ? FORGE_L(OP_SGDM, ST_F32, false) : FORGE_L(OP_SGDM, ST_BF16, false);
     default:
-        return launch_wgrad<IT, OP_DW, ST_F32, false, MAN>(a, b, p, grid, s);
+        return FORGE_L(OP_DW, ST_F32, false);
     }
+#undef FORGE_L
 }
 
 template <int IT, int NP>
-cudaError_t dispatch_pair(int op, int st, const CUtensorMap& a, const CUtensorMap& b,
-                          const Params& p, int64_t grid, cudaStream_t s)
+cudaError_t dispatch_pair(int op, int st, bool grouped, const Maps& m, const Params& p,
+                          int64_t grid, cudaStream_t s)
 {
+#define FORGE_L(OPV, STV, G) launch_wgrad_pair<IT, OPV, STV, NP, G>(m.a, m.b, m.a1, m.b1, p, grid, s)
+    if constexpr (NP == 1) {
+        if (grouped)
+            return st == ST_F32 ? FORGE_L(OP_ADAMW, ST_F32, true) : FORGE_L(OP_ADAMW, ST_BF16, true);
+    }
     switch (op) {
     case OP_ADAMW:
-        return st == ST_F32 ? launch_wgrad_pair<IT, OP_ADAMW, ST_F32, NP>(a, b, p, grid, s)
-                            : launch_wgrad_pair<IT, OP_ADAMW, ST_BF16, NP>(a, b, p, grid, s);
+        return st == ST_F32 ? FORGE_L(OP_ADAMW, ST_F32, false) : FORGE_L(OP_ADAMW, ST_BF16, false);
     case OP_SGDM:
-        return st == ST_F32 ? launch_wgrad_pair<IT, OP_SGDM, ST_F32, NP>(a, b, p, grid, s)
-                            : launch_wgrad_pair<IT, OP_SGDM, ST_BF16, NP>(a, b, p, grid, s);
+        return st == ST_F32 ? FORGE_L(OP_SGDM, ST_F32, false) : FORGE_L(OP_SGDM, ST_BF16, false);
     default:
-        return launch_wgrad_pair<IT, OP_DW, ST_F32, NP>(a, b, p, grid, s);
+        return FORGE_L(OP_DW, ST_F32, false);
     }
+#undef FORGE_L
 }
 
 // Kernel form: 0 = one CTA per 128 x 256 tile; 1 = CTA pairs on 256 x 256
 // tiles; 2 = clusters of two pairs (512 x 256) sharing X through multicast.
-// Pairs serve dense calls whose operands TMA can address and whose d_out
-// exceeds 128; the two-pair form moves a quarter fewer operand bytes through
-// L2 but measured no faster on GB300, so it runs only on request.
-// FORGE_KERNEL = single | pair | quad (read on every call) overrides the
-// automatic choice where that form applies.
+// Pairs serve calls whose operands TMA can address and whose d_out exceeds
+// 128, dense or grouped; the two-pair form (dense only) moves a quarter fewer
+// operand bytes through L2 but measured no faster on GB300, so it runs only
+// on request.  FORGE_KERNEL = single | pair | quad (read on every call)
+// overrides the automatic choice where that form applies.
 int kernel_form(const Params& p, bool grouped, bool manual)
 {
-    if (grouped || manual) return 0;
+    if (manual) return 0;
     const char* e = std::getenv("FORGE_KERNEL");
     if (e && std::strcmp(e, "single") == 0) return 0;
     if (e && std::strcmp(e, "pair") == 0) return 1;
-    if (e && std::strcmp(e, "quad") == 0) return 2;
+    if (e && std::strcmp(e, "quad") == 0) return grouped ? 1 : 2;
     return p.M > BM ? 1 : 0;
 }
 
@@ -259,16 +270,21 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
 
     const bool man = p.manual_a || p.manual_b;
     const int form = kernel_form(p, grouped, man);
-    CUtensorMap tmA, tmB;
-    std::memset(&tmA, 0, sizeof tmA);
-    std::memset(&tmB, 0, sizeof tmB);
+    Maps maps;
+    std::memset(&maps, 0, sizeof maps);
     p.has_maps = rows > 0 ? 1 : 0;
     if (rows > 0) {
-        if (!p.manual_a && (st = encode_operand(&tmA, dY, in_dtype, p.M, rows)) != FORGE_OK)
+        if (!p.manual_a && (st = encode_operand(&maps.a, dY, in_dtype, p.M, rows)) != FORGE_OK)
             return st;
         // two pairs fetch half of each X box's k rows apiece
-        if (!p.manual_b &&
-            (st = encode_operand(&tmB, X, in_dtype, p.N, rows, form == 2 ? 2 : 1)) != FORGE_OK)
+        if (!p.manual_b && (st = encode_operand(&maps.b, X, in_dtype, p.N, rows,
+                                                form == 2 ? 2 : 1)) != FORGE_OK)
+            return st;
+        if (grouped && !p.manual_a &&
+            (st = encode_operand(&maps.a1, dY, in_dtype, p.M, rows, 0)) != FORGE_OK)
+            return st;
+        if (grouped && !p.manual_b &&
+            (st = encode_operand(&maps.b1, X, in_dtype, p.N, rows, 0)) != FORGE_OK)
             return st;
     }
     const int64_t tile_m = form == 2 ? 4 * BM : (form == 1 ? 2 * BM : BM);
@@ -288,21 +304,21 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
         // the launcher sizes the grid from the resident-cluster limit
         if (form == 1)
             e = in_dtype == FORGE_BF16
-                    ? dispatch_pair<IN_BF16, 1>(op, ist, tmA, tmB, p, total, stream)
-                    : dispatch_pair<IN_E4M3, 1>(op, ist, tmA, tmB, p, total, stream);
+                    ? dispatch_pair<IN_BF16, 1>(op, ist, grouped, maps, p, total, stream)
+                    : dispatch_pair<IN_E4M3, 1>(op, ist, grouped, maps, p, total, stream);
         else
             e = in_dtype == FORGE_BF16
-                    ? dispatch_pair<IN_BF16, 2>(op, ist, tmA, tmB, p, total, stream)
-                    : dispatch_pair<IN_E4M3, 2>(op, ist, tmA, tmB, p, total, stream);
+                    ? dispatch_pair<IN_BF16, 2>(op, ist, false, maps, p, total, stream)
+                    : dispatch_pair<IN_E4M3, 2>(op, ist, false, maps, p, total, stream);
         return from_cuda(e);
     }
     const int grid = static_cast<int>(total < dev->sms ? total : dev->sms);
     if (in_dtype == FORGE_BF16)
-        e = man ? dispatch_op<IN_BF16, true>(op, ist, grouped, tmA, tmB, p, grid, stream)
-                : dispatch_op<IN_BF16, false>(op, ist, grouped, tmA, tmB, p, grid, stream);
+        e = man ? dispatch_op<IN_BF16, true>(op, ist, grouped, maps, p, grid, stream)
+                : dispatch_op<IN_BF16, false>(op, ist, grouped, maps, p, grid, stream);
     else
-        e = man ? dispatch_op<IN_E4M3, true>(op, ist, grouped, tmA, tmB, p, grid, stream)
-                : dispatch_op<IN_E4M3, false>(op, ist, grouped, tmA, tmB, p, grid, stream);
+        e = man ? dispatch_op<IN_E4M3, true>(op, ist, grouped, maps, p, grid, stream)
+                : dispatch_op<IN_E4M3, false>(op, ist, grouped, maps, p, grid, stream);
     return from_cuda(e);
 }
 

@@ -477,6 +477,61 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, 
     }
 }
 
+// ------------------------------------------------------------------ grouped set-up
+
+// Copies the expert offsets into shared memory, validates them and ranks the
+// experts by token count (descending, ties by index) without atomics.  Every
+// thread of the CTA calls it; it returns false for the whole CTA (after the
+// first CTA records FORGE_ERR_INVALID_ARG) when the offsets are invalid.
+__device__ __forceinline__ bool grouped_setup(const Params& p, int32_t* s_offs, int32_t* s_order,
+                                              volatile int* s_bad)
+{
+    for (int i = threadIdx.x; i <= p.E; i += kThreads) s_offs[i] = p.offsets[i];
+    if (threadIdx.x == 0) *s_bad = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < p.E; e += kThreads) {
+        const int32_t a = s_offs[e], b = s_offs[e + 1];
+        if (a < 0 || b < a || static_cast<int64_t>(b) > p.T_max) *s_bad = 1;
+    }
+    __syncthreads();
+    if (*s_bad) {
+        if (threadIdx.x == 0 && blockIdx.x == 0)
+            *reinterpret_cast<volatile int*>(p.status) = kDevInvalidArg;
+        return false;
+    }
+    for (int e = threadIdx.x; e < p.E; e += kThreads) {
+        const int32_t ke = s_offs[e + 1] - s_offs[e];
+        int32_t rank = 0;
+        for (int f = 0; f < p.E; ++f) {
+            const int32_t kf = s_offs[f + 1] - s_offs[f];
+            rank += (kf > ke) || (kf == ke && f < e);
+        }
+        s_order[rank] = e;
+    }
+    return true;
+}
+
+// A k-block that runs past the current expert's tokens (grouped calls):
+// rows [ky, ky + BK) of NBOX 128-byte column blocks from column mn0 are
+// fetched four at a time through a one-row-box map, each row at or past kend
+// replaced by the out-of-range index oob so that TMA writes zeros there.  Both
+// operands are loaded this way, so another expert's tokens never enter the
+// product (not even as 0 x inf).  issue(byte offset, column, rows[4]) makes
+// one copy.
+template <int BK, int NBOX, int BOX_MN, int BOX_BYTES, class Issue>
+__device__ __forceinline__ void gather_block(int32_t mn0, int32_t ky, int32_t kend, int32_t oob,
+                                             Issue&& issue)
+{
+#pragma unroll 1
+    for (int r = 0; r < BK; r += 4) {
+        int32_t y[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) y[j] = ky + r + j < kend ? ky + r + j : oob;
+#pragma unroll
+        for (int i = 0; i < NBOX; ++i) issue(i * BOX_BYTES + r * 128, mn0 + i * BOX_MN, y);
+    }
+}
+
 // ------------------------------------------------------------------ cp.async loader
 
 constexpr int kLoaderWarp0 = 2;  // warps 2 and 3
@@ -534,8 +589,10 @@ __device__ __forceinline__ void load_block_cp_async(uint8_t* stage, const uint8_
 
 template <int IT, int OP, int ST, bool GROUPED, bool MANUAL>
 __global__ void __launch_bounds__(kThreads, 1)
-    forge_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,  // dY
-                       const __grid_constant__ CUtensorMap tmB,  // X
+    forge_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,   // dY
+                       const __grid_constant__ CUtensorMap tmB,   // X
+                       const __grid_constant__ CUtensorMap tmA1,  // dY, one-row boxes (grouped)
+                       const __grid_constant__ CUtensorMap tmB1,  // X, one-row boxes (grouped)
                        const Params p)
 {
     using TR = InTraits<IT>;
@@ -580,31 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if constexpr (GROUPED) {
-        // Copy the expert offsets and validate them; rank experts by token
-        // count (descending, ties by index) without atomics.
-        for (int i = threadIdx.x; i <= p.E; i += kThreads) s_offs[i] = p.offsets[i];
-        __syncthreads();
-        __shared__ int bad;
-        if (threadIdx.x == 0) bad = 0;
-        __syncthreads();
-        for (int e = threadIdx.x; e < p.E; e += kThreads) {
-            const int32_t a = s_offs[e], b = s_offs[e + 1];
-            if (a < 0 || b < a || static_cast<int64_t>(b) > p.T_max) bad = 1;
-        }
-        __syncthreads();
-        if (bad) {
-            if (threadIdx.x == 0 && blockIdx.x == 0) *reinterpret_cast<volatile int*>(p.status) = kDevInvalidArg;
-            return;  // uniform across the CTA; nothing allocated yet
-        }
-        for (int e = threadIdx.x; e < p.E; e += kThreads) {
-            const int32_t ke = s_offs[e + 1] - s_offs[e];
-            int32_t rank = 0;
-            for (int f = 0; f < p.E; ++f) {
-                const int32_t kf = s_offs[f + 1] - s_offs[f];
-                rank += (kf > ke) || (kf == ke && f < e);
-            }
-            s_order[rank] = e;
-        }
+        if (!grouped_setup(p, s_offs, s_order, abort_flag + 1)) return;  // nothing allocated yet
     }
 
     if (warp == 0 && lane == 0 && p.has_maps) {
@@ -659,17 +692,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* sa = smem + s * kStageBytes;
                     uint8_t* sb = sa + kStageA;
                     const int32_t ky = static_cast<int32_t>(k);
+                    const bool partial = GROUPED && tl.k_end - k < BK;
+                    const int32_t kend = static_cast<int32_t>(tl.k_end);
+                    const int32_t oob = static_cast<int32_t>(p.T_max);
                     if (tma_a) {
+                        if (partial) {
+                            gather_block<BK, kABoxes, TR::box_mn, kBoxBytes>(
+                                tl.m0, ky, kend, oob, [&](int off, int32_t x, const int32_t* y) {
+                                    ptx::tma_gather4_2d(sa + off, &tmA1, &full[s], x, y[0], y[1],
+                                                        y[2], y[3]);
+                                });
+                        } else {
 #pragma unroll
-                        for (int i = 0; i < kABoxes; ++i)
-                            ptx::tma_load_2d_hint(sa + i * kBoxBytes, &tmA, &full[s],
-                                                  tl.m0 + i * TR::box_mn, ky, pol);
+                            for (int i = 0; i < kABoxes; ++i)
+                                ptx::tma_load_2d_hint(sa + i * kBoxBytes, &tmA, &full[s],
+                                                      tl.m0 + i * TR::box_mn, ky, pol);
+                        }
                     }
                     if (tma_b) {
+                        if (partial) {
+                            gather_block<BK, kBBoxes, TR::box_mn, kBoxBytes>(
+                                tl.n0, ky, kend, oob, [&](int off, int32_t x, const int32_t* y) {
+                                    ptx::tma_gather4_2d(sb + off, &tmB1, &full[s], x, y[0], y[1],
+                                                        y[2], y[3]);
+                                });
+                        } else {
 #pragma unroll
-                        for (int i = 0; i < kBBoxes; ++i)
-                            ptx::tma_load_2d(sb + i * kBoxBytes, &tmB, &full[s],
-                                             tl.n0 + i * TR::box_mn, ky);
+                            for (int i = 0; i < kBBoxes; ++i)
+                                ptx::tma_load_2d(sb + i * kBoxBytes, &tmB, &full[s],
+                                                 tl.n0 + i * TR::box_mn, ky);
+                        }
                     }
                     issued_mask |= 1u << s;
                     last_parity = (last_parity & ~(1u << s)) | (ph << s);
@@ -717,27 +769,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
                     ok = wait_bounded(&full[s], ph, abort_flag, p);
                     if (!ok) break;
-                    if constexpr (GROUPED) {
-                        // Rows past this expert's last token belong to the next
-                        // expert (TMA zero-fills only outside the tensor), so
-                        // they are cleared in the A operand before the tensor
-                        // core reads the stage.  With MN-major 128-byte swizzle
-                        // each k row is one whole 128-byte line per column
-                        // block, so a row is cleared without undoing the swizzle.
-                        const int64_t valid = tl.k_end - k;
-                        if (valid < BK) {
-                            ptx::fence_proxy_async_smem();  // after the TMA writes
-                            for (int r = static_cast<int>(valid); r < BK; ++r)
-#pragma unroll
-                                for (int i = 0; i < kABoxes; ++i) {
-                                    uint4* row = reinterpret_cast<uint4*>(
-                                        smem + s * kStageBytes + i * kBoxBytes + r * 128);
-#pragma unroll
-                                    for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
-                                }
-                            ptx::fence_proxy_async_smem();  // before the tensor core reads
-                        }
-                    }
                     const uint32_t sa = ptx::smem_addr(smem + s * kStageBytes);
                     const uint32_t sb = sa + kStageA;
 #pragma unroll
@@ -840,7 +871,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ CTA-pair kernel
 
-// Dense form on CTA pairs.  A pair owns a 256 (m) x 256 (n) tile: CTA r of
+// CTA-pair form (dense, and grouped with one expert per tile).  A pair owns a
+// 256 (m) x 256 (n) tile: CTA r of
 // the pair loads the 128 rows m0 + 128 r .. of dY and the 128 columns
 // n0 + 128 r .. of X, and the even CTA issues tcgen05.mma.cta_group::2, which
 // reads the A half of each CTA and both B halves and leaves each CTA's 128 x
@@ -869,13 +901,16 @@ constexpr int kPairStageB = 16384;  // this CTA's 128 columns of X x BK
 constexpr int kPairStageBytes = kPairStageA + kPairStageB;
 static_assert(kPairStages * kPairStageBytes <= kSmemBarOffset, "pair ring fits the stage area");
 
-template <int IT, int OP, int ST, int NPAIR>
+template <int IT, int OP, int ST, int NPAIR, bool GROUPED>
 __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
-    forge_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,  // dY
-                            const __grid_constant__ CUtensorMap tmB,  // X, boxes of BK / NPAIR rows
+    forge_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,   // dY
+                            const __grid_constant__ CUtensorMap tmB,   // X, boxes of BK / NPAIR rows
+                            const __grid_constant__ CUtensorMap tmA1,  // dY, one-row boxes (grouped)
+                            const __grid_constant__ CUtensorMap tmB1,  // X, one-row boxes (grouped)
                             const Params p)
 {
     static_assert(NPAIR == 1 || NPAIR == 2, "one or two pairs per cluster");
+    static_assert(!GROUPED || NPAIR == 1, "grouped calls use single pairs");
     using TR = InTraits<IT>;
     constexpr int BK = TR::BK;
     constexpr int kBoxBytes = TR::box_mn * TR::esize * BK;
@@ -897,6 +932,8 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int32_t* s_offs = reinterpret_cast<int32_t*>(smem + kSmemSchedOffset);
+    int32_t* s_order = s_offs + (kMaxExperts + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -923,6 +960,10 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         ptx::fence_mbarrier_init();
     }
+    if constexpr (GROUPED) {
+        // both CTAs of a pair read the same offsets, so they return together
+        if (!grouped_setup(p, s_offs, s_order, abort_flag + 1)) return;
+    }
     if (warp == 0 && lane == 0 && p.has_maps) {
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB);
@@ -943,10 +984,10 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
     sc.m_off = static_cast<int32_t>(crank) * BM;
     sc.band = p.raster_band;
     sc.per_expert = p.tiles_m * p.tiles_n;
-    sc.total = sc.per_expert;
-    sc.set_share(blockIdx.x / (2 * NPAIR), gridDim.x / (2 * NPAIR), 0);
-    sc.offs = nullptr;
-    sc.order = nullptr;
+    sc.total = sc.per_expert * p.E;
+    sc.set_share(blockIdx.x / (2 * NPAIR), gridDim.x / (2 * NPAIR), GROUPED ? 1 : 0);
+    sc.offs = GROUPED ? s_offs : nullptr;
+    sc.order = GROUPED ? s_order : nullptr;
     sc.K = p.K;
     sc.MN = p.M * p.N;
 
@@ -973,20 +1014,36 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
                     uint8_t* sb = sa + kPairStageA;
                     const uint32_t bar = full0 + s * 8;
                     const int32_t ky = static_cast<int32_t>(k);
-#pragma unroll
-                    for (int i = 0; i < kABoxes; ++i)
-                        ptx::tma_load_2d_pair_hint(sa + i * kBoxBytes, &tmA, bar,
-                                                   tl.m0 + i * TR::box_mn, ky, pol);
                     const int32_t nb = tl.n0 + static_cast<int32_t>(rank) * (BN / 2);
+                    if (GROUPED && tl.k_end - k < BK) {
+                        const int32_t kend = static_cast<int32_t>(tl.k_end);
+                        const int32_t oob = static_cast<int32_t>(p.T_max);
+                        gather_block<BK, kABoxes, TR::box_mn, kBoxBytes>(
+                            tl.m0, ky, kend, oob, [&](int off, int32_t x, const int32_t* y) {
+                                ptx::tma_gather4_2d_pair(sa + off, &tmA1, bar, x, y[0], y[1], y[2],
+                                                         y[3]);
+                            });
+                        gather_block<BK, kBBoxes, TR::box_mn, kBoxBytes>(
+                            nb, ky, kend, oob, [&](int off, int32_t x, const int32_t* y) {
+                                ptx::tma_gather4_2d_pair(sb + off, &tmB1, bar, x, y[0], y[1], y[2],
+                                                         y[3]);
+                            });
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < kBBoxes; ++i) {
-                        if constexpr (NPAIR == 1) {
-                            ptx::tma_load_2d_pair(sb + i * kBoxBytes, &tmB, bar, nb + i * TR::box_mn, ky);
-                        } else {
-                            // rows [pair_id * kBRows, +kBRows) of this B box, to both pairs
-                            const int r0 = static_cast<int>(pair_id) * kBRows;
-                            ptx::tma_load_2d_pair_mc(sb + i * kBoxBytes + r0 * 128, &tmB, bar,
-                                                     nb + i * TR::box_mn, ky + r0, b_mask);
+                        for (int i = 0; i < kABoxes; ++i)
+                            ptx::tma_load_2d_pair_hint(sa + i * kBoxBytes, &tmA, bar,
+                                                       tl.m0 + i * TR::box_mn, ky, pol);
+#pragma unroll
+                        for (int i = 0; i < kBBoxes; ++i) {
+                            if constexpr (NPAIR == 1) {
+                                ptx::tma_load_2d_pair(sb + i * kBoxBytes, &tmB, bar,
+                                                      nb + i * TR::box_mn, ky);
+                            } else {
+                                // rows [pair_id * kBRows, +kBRows) of this B box, to both pairs
+                                const int r0 = static_cast<int>(pair_id) * kBRows;
+                                ptx::tma_load_2d_pair_mc(sb + i * kBoxBytes + r0 * 128, &tmB, bar,
+                                                         nb + i * TR::box_mn, ky + r0, b_mask);
+                            }
                         }
                     }
                     issued_mask |= 1u << s;

@@ -12,29 +12,31 @@ namespace forge {
 // Sets the kernel's shared-memory limit on the current device (once per
 // device) and launches it on `stream`.
 template <int IT, int OP, int ST, bool GROUPED, bool MANUAL>
-cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
-                         int grid, cudaStream_t stream);
+cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmA1,
+                         const CUtensorMap& tmB1, const Params& p, int grid, cudaStream_t stream);
 
 // Same for the CTA-pair kernels.  The grid is sized from the number of
 // clusters of 2 * NPAIR CTAs that can be resident at once (a cluster must fit
 // in one GPC), never more than `total_tiles` clusters.
-template <int IT, int OP, int ST, int NPAIR>
-cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
+template <int IT, int OP, int ST, int NPAIR, bool GROUPED>
+cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                              const CUtensorMap& tmA1, const CUtensorMap& tmB1, const Params& p,
                               int64_t total_tiles, cudaStream_t stream);
 
 }  // namespace forge
 
 #define FORGE_DEFINE_LAUNCH_PAIR()                                                             \
     namespace forge {                                                                          \
-    template <int IT, int OP, int ST, int NPAIR>                                               \
+    template <int IT, int OP, int ST, int NPAIR, bool GROUPED>                                 \
     cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,              \
+                                  const CUtensorMap& tmA1, const CUtensorMap& tmB1,            \
                                   const Params& p, int64_t total_tiles, cudaStream_t stream)   \
     {                                                                                          \
         static int max_clusters[64] = {0};                                                     \
         int dev = 0;                                                                           \
         cudaError_t e = cudaGetDevice(&dev);                                                   \
         if (e != cudaSuccess) return e;                                                        \
-        auto kern = forge_wgrad_pair_kernel<IT, OP, ST, NPAIR>;                                \
+        auto kern = forge_wgrad_pair_kernel<IT, OP, ST, NPAIR, GROUPED>;                       \
         int& mc = max_clusters[dev & 63];                                                      \
         if (__atomic_load_n(&mc, __ATOMIC_ACQUIRE) == 0) {                                     \
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
@@ -51,26 +53,29 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, co
             __atomic_store_n(&mc, n, __ATOMIC_RELEASE);                                        \
         }                                                                                      \
         const int64_t nc = total_tiles < mc ? total_tiles : mc;                                \
-        kern<<<static_cast<int>(2 * NPAIR * nc), kThreads, kSmemAlloc, stream>>>(tmA, tmB, p); \
+        kern<<<static_cast<int>(2 * NPAIR * nc), kThreads, kSmemAlloc, stream>>>(              \
+            tmA, tmB, tmA1, tmB1, p);                                                          \
         return cudaGetLastError();                                                             \
     }                                                                                          \
     }
 
-#define FORGE_INSTANTIATE_PAIR(IT, OP, ST, NPAIR)                                              \
-    template cudaError_t forge::launch_wgrad_pair<IT, OP, ST, NPAIR>(                          \
-        const CUtensorMap&, const CUtensorMap&, const forge::Params&, int64_t, cudaStream_t);
+#define FORGE_INSTANTIATE_PAIR(IT, OP, ST, NPAIR, G)                                           \
+    template cudaError_t forge::launch_wgrad_pair<IT, OP, ST, NPAIR, G>(                       \
+        const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,        \
+        const forge::Params&, int64_t, cudaStream_t);
 
 #define FORGE_DEFINE_LAUNCH()                                                                  \
     namespace forge {                                                                          \
     template <int IT, int OP, int ST, bool GROUPED, bool MANUAL>                               \
-    cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,  \
-                             int grid, cudaStream_t stream)                                    \
+    cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB,                   \
+                             const CUtensorMap& tmA1, const CUtensorMap& tmB1,                 \
+                             const Params& p, int grid, cudaStream_t stream)                   \
     {                                                                                          \
         static unsigned long long attr_done = 0; /* one bit per device ordinal < 64 */         \
         int dev = 0;                                                                           \
         cudaError_t e = cudaGetDevice(&dev);                                                   \
         if (e != cudaSuccess) return e;                                                        \
-        auto kern = forge_wgrad_kernel<IT, OP, ST, GROUPED, MANUAL>;                                   \
+        auto kern = forge_wgrad_kernel<IT, OP, ST, GROUPED, MANUAL>;                           \
         const unsigned long long bit = 1ull << (dev & 63);                                     \
         if (!(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {                          \
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
@@ -78,11 +83,12 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, co
             if (e != cudaSuccess) return e;                                                    \
             __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);                              \
         }                                                                                      \
-        kern<<<grid, kThreads, kSmemAlloc, stream>>>(tmA, tmB, p);                             \
+        kern<<<grid, kThreads, kSmemAlloc, stream>>>(tmA, tmB, tmA1, tmB1, p);                 \
         return cudaGetLastError();                                                             \
     }                                                                                          \
     }
 
 #define FORGE_INSTANTIATE(IT, OP, ST, G, MAN)                                                  \
     template cudaError_t forge::launch_wgrad<IT, OP, ST, G, MAN>(                              \
-        const CUtensorMap&, const CUtensorMap&, const forge::Params&, int, cudaStream_t);
+        const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,        \
+        const forge::Params&, int, cudaStream_t);

@@ -92,6 +92,21 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// Gather four rows y0..y3 (each one box row of 128 bytes starting at x)
+// into consecutive 128-byte rows at dst; a row index outside the tensor
+// reads zeros.  The map's box is one row high.
+__device__ __forceinline__ void tma_gather4_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                               int32_t x, int32_t y0, int32_t y1, int32_t y2,
+                                               int32_t y3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+        "r"(smem_addr(bar))
+        : "memory");
+}
+
 // Same with an L2 cache-policy hint (createpolicy value).
 __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar,
                                                  int32_t x, int32_t y, uint64_t policy)
@@ -333,6 +348,21 @@ __device__ __forceinline__ void tma_load_2d_pair_mc(void* dst, const CUtensorMap
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr), "h"(cta_mask)
+        : "memory");
+}
+
+// Pair form of the four-row gather (completion counted on a barrier that may
+// live in the peer CTA).
+__device__ __forceinline__ void tma_gather4_2d_pair(void* dst, const CUtensorMap* map,
+                                                    uint32_t bar_cluster_addr, int32_t x,
+                                                    int32_t y0, int32_t y1, int32_t y2, int32_t y3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+        ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+        "r"(bar_cluster_addr)
         : "memory");
 }
 
