@@ -14,13 +14,14 @@
 // lanes cover 32 consecutive m: every global access of the epilogue is a
 // fully coalesced 128-byte (fp32) or 64-byte (bf16) row segment.
 //
-// Roles (384 threads, one CTA per SM, persistent over a static tile list):
+// Roles (384 or 640 threads, one CTA per SM, persistent over a static tile list):
 //   warp 0      TMA producer: K-blocks of dY and X into a 4-stage ring
 //   warp 1      TMEM allocator; lane 0 alone issues tcgen05.mma into one of
 //               two 128x256 fp32 accumulators (512 TMEM columns)
-//   warps 4-11  epilogue: tcgen05.ld the accumulator, apply AdamW / SGD-m /
+//   warps 2-3   cp.async loader for operands TMA cannot address
+//   warps 4-    epilogue: tcgen05.ld the accumulator, apply AdamW / SGD-m /
 //               plain store, write W and the state back; two warpgroups
-//               split the 256 columns
+//               (dense calls) or four (grouped calls) split the 256 columns
 // Each output tile is computed by exactly one CTA over the whole K in a
 // fixed order: no split-K and no atomics, so results are bitwise
 // reproducible and independent of the schedule (P1).
@@ -42,9 +43,7 @@ constexpr int kDevOk = 0;
 constexpr int kDevInvalidArg = -1;
 constexpr int kDevTimeout = -6;
 
-constexpr int kThreads = 384;
-constexpr int kEpiWarp0 = 4;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarp0 = 4;  // warps 0-3: producer, MMA issuer, cp.async loader
 constexpr int BM = 128;  // m (d_out) per tile = UMMA M = TMEM lanes
 constexpr int BN = 256;  // n (d_in) per tile  = UMMA N = TMEM columns per accumulator
 constexpr int kStages = 4;
@@ -55,11 +54,34 @@ constexpr int kTmemCols = 512;  // two 256-column accumulators
 constexpr int kMaxExperts = 1024;
 constexpr int kSmemBarOffset = kStages * kStageBytes;
 constexpr int kSmemSchedOffset = kSmemBarOffset + 256;
-// per epilogue warp: one 16 (n) x 32 (m) fp32 chunk of the accumulator, used
-// to hand each lane four consecutive m of one n (see the epilogue)
-constexpr int kStageFloats = 16 * 32;
+
+// Epilogue geometry for EW epilogue warps.  Warp (q, grp) owns TMEM lane
+// quarter q and warp_cols accumulator columns, walked in chunks of
+// chunk_cols (n) x 32 (m); after a pass through shared memory a lane holds
+// four consecutive m for chunk_n consecutive n.  Sixteen warps with 8-column
+// chunks keep more state loads in flight per SM (the epilogue-bound grouped
+// calls); eight warps with 16-column chunks leave more issue slots to the
+// producer and the MMA issuer (the MMA-bound dense calls).
+template <int EW>
+struct Epi {
+    static_assert(EW == 8 || EW == 16, "two or four warpgroups");
+    static constexpr int warps = EW;
+    static constexpr int threads = (kEpiWarp0 + EW) * 32;
+    static constexpr int groups = EW / 4;  // column groups per TMEM lane quarter
+    static constexpr int warp_cols = BN / groups;
+    static constexpr int chunk_cols = EW == 16 ? 8 : 16;
+    static constexpr int chunk_n = chunk_cols / 4;
+    static constexpr int chunks = warp_cols / chunk_cols;
+    static constexpr int stage_floats = chunk_cols * 32;  // per warp
+};
+template <bool GROUPED>
+using EpiFor = Epi<GROUPED ? 16 : 8>;
+constexpr int kStageBytesEpi = 16384;  // the epilogue warps' shared-memory stages
+static_assert(Epi<8>::warps * Epi<8>::stage_floats * 4 == kStageBytesEpi &&
+                  Epi<16>::warps * Epi<16>::stage_floats * 4 == kStageBytesEpi,
+              "one stage area for both geometries");
 constexpr int kSmemStageOffset = (kSmemSchedOffset + 4 * (2 * kMaxExperts + 2) + 127) & ~127;
-constexpr int kSmemBytes = kSmemStageOffset + kEpiWarps * kStageFloats * 4;
+constexpr int kSmemBytes = kSmemStageOffset + kStageBytesEpi;
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
 
 template <int IT>
@@ -280,11 +302,12 @@ struct StateIO<ST_BF16> {
 
 // One lane's share of a 16 (n) x 32 (m) accumulator chunk: four n rows of
 // four consecutive m each; element [jj * 4 + i] is (n = 4 ns + jj, m = 4 mg + i).
+template <int CN>
 struct Chunk {
-    float g[16];
-    float w[16];
-    float a[16];  // m (AdamW) or momentum (SGD)
-    float b[16];  // v (AdamW)
+    float g[4 * CN];
+    float w[4 * CN];
+    float a[4 * CN];  // m (AdamW) or momentum (SGD)
+    float b[4 * CN];  // v (AdamW)
 };
 
 // The optimizer step on four consecutive parameters of one row.
@@ -313,35 +336,43 @@ __device__ __forceinline__ void step4(const Params& p, const float* g, float* w,
 
 // ------------------------------------------------------------------ epilogue role
 
-// Epilogue warps 4..11 of one CTA.  Warp (q, half) owns TMEM lanes
-// 32q..32q+31 (m) and columns 128 half .. 128 half + 127 (n) of the
-// accumulator, walked in 16-column chunks.  Each chunk goes TMEM -> registers
-// (lane = m) -> a 2 KB smem stage -> registers again with lane (mg, ns)
-// holding m = 4 mg .. 4 mg + 3 for n = 4 ns .. 4 ns + 3, so every global access
-// is a 16-byte (fp32) or 8-byte (bf16) vector and a warp instruction covers
-// four 128-byte (or 64-byte) row segments.  The state loads of chunk c+1 are
-// in flight while chunk c is updated and stored.  `release_acc(b)` hands
-// accumulator buffer b back to the MMA issuer once it has been read.
-template <int IT, int OP, int ST, class ReleaseAcc>
+// Epilogue warps of one CTA (EC::warps of them, from warp kEpiWarp0).  Warp
+// (q, grp) owns TMEM lanes 32q..32q+31 (m) and columns EC::warp_cols grp ..
+// EC::warp_cols (grp + 1) - 1 (n) of the accumulator, walked in chunks.  Each
+// chunk goes TMEM -> registers (lane = m) -> a small smem stage -> registers
+// again with lane (mg, ns) holding m = 4 mg .. 4 mg + 3 for n = chunk_n ns ..
+// chunk_n ns + chunk_n - 1, so every global access is a 16-byte (fp32) or
+// 8-byte (bf16) vector and a warp instruction covers four 128-byte (or
+// 64-byte) row segments.  The state loads of chunk c+1 are in flight while
+// chunk c is updated and stored.  `release_acc(b)` hands accumulator buffer b
+// back to the MMA issuer once it has been read.
+// One chunk of TMEM columns (the overload matches the chunk width).
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[8])
+{
+    ptx::tmem_ld_32x32b_x8(taddr, r);
+}
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[16])
+{
+    ptx::tmem_ld_32x32b_x16(taddr, r);
+}
+
+template <int IT, int OP, int ST, class EC, class ReleaseAcc>
 __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, uint8_t* smem,
                                               uint64_t* tfull, uint32_t tmem_base,
                                               volatile int* abort_flag, int warp, int lane,
                                               ReleaseAcc release_acc)
 {
-        // Warp (q, half) owns TMEM lanes 32q..32q+31 (m) and columns
-    // 128 half .. 128 half + 127 (n) of the accumulator, walked in 16-column
-    // chunks.  Each chunk goes TMEM -> registers (lane = m) -> a 2 KB smem
-    // stage -> registers again with lane (mg, ns) holding m = 4 mg .. 4 mg + 3
-    // for n = 4 ns .. 4 ns + 3, so every global access is a 16-byte (fp32)
-    // or 8-byte (bf16) vector and a warp instruction covers four 128-byte
-    // (or 64-byte) row segments.  The state loads of chunk c+1 are in
-    // flight while chunk c is updated and stored.
     const int ew = warp - kEpiWarp0;
     const int q = warp & 3;     // TMEM lane quarter this warp may access
-    const int half = ew >> 2;   // which 128 of the 256 columns
+    const int grp = ew >> 2;    // which EC::warp_cols of the 256 columns
+    constexpr int kWarpCols = EC::warp_cols;
+    constexpr int kChunkCols = EC::chunk_cols;
+    constexpr int kChunkN = EC::chunk_n;
+    constexpr int kChunks = EC::chunks;
+    using Chunk = forge::Chunk<kChunkN>;
     const int mg = lane & 7;
     const int ns = lane >> 3;
-    float* stg = reinterpret_cast<float*>(smem + kSmemStageOffset) + ew * kStageFloats;
+    float* stg = reinterpret_cast<float*>(smem + kSmemStageOffset) + ew * EC::stage_floats;
     const int64_t M = p.M;
     const int64_t N = p.N;
     float gscale = 1.0f;
@@ -360,10 +391,14 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, 
         const int64_t mrow = tl.m0 + 32 * q + 4 * mg;  // this lane's first m
         const int mvalid = mrow >= M ? 0 : (mrow + 4 <= M ? 4 : static_cast<int>(M - mrow));
         const bool vec = p.vec_ok && mvalid == 4;
-        const int64_t n_first = tl.n0 + 128 * half;
+        const int64_t n_first = tl.n0 + kWarpCols * grp;
         const int64_t left = N - n_first;
-        const int nchunks = left <= 0 ? 0 : (left >= 128 ? 8 : static_cast<int>((left + 15) / 16));
-        const uint32_t tcol = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN + 128 * half;
+        const int nchunks =
+            left <= 0 ? 0
+                      : (left >= kWarpCols ? kChunks
+                                           : static_cast<int>((left + kChunkCols - 1) / kChunkCols));
+        const uint32_t tcol =
+            tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN + kWarpCols * grp;
 
         auto release = [&]() {
             ptx::tc_fence_before();
@@ -373,18 +408,19 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, 
 
         auto fetch = [&](int c, Chunk& ch) {
             if (has_acc) {
-                uint32_t r[16];
-                ptx::tmem_ld_32x32b_x16(tcol + 16 * c, r);
+                uint32_t r[kChunkCols];
+                tmem_ld_chunk(tcol + kChunkCols * c, r);
                 ptx::tmem_ld_wait();
                 if (c == nchunks - 1) release();  // accumulator fully read
                 __syncwarp();  // previous chunk's stage reads are complete
 #pragma unroll
-                for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = __uint_as_float(r[j]) * gscale;
+                for (int j = 0; j < kChunkCols; ++j)
+                    stg[j * 32 + lane] = __uint_as_float(r[j]) * gscale;
                 __syncwarp();
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
+                for (int jj = 0; jj < kChunkN; ++jj) {
                     const float4 v =
-                        *reinterpret_cast<const float4*>(stg + (4 * ns + jj) * 32 + 4 * mg);
+                        *reinterpret_cast<const float4*>(stg + (kChunkN * ns + jj) * 32 + 4 * mg);
                     ch.g[jj * 4 + 0] = v.x;
                     ch.g[jj * 4 + 1] = v.y;
                     ch.g[jj * 4 + 2] = v.z;
@@ -392,12 +428,12 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, 
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) ch.g[j] = 0.0f;
+                for (int j = 0; j < 4 * kChunkN; ++j) ch.g[j] = 0.0f;
             }
             if constexpr (OP != OP_DW) {
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const int64_t n = n_first + 16 * c + 4 * ns + jj;
+                for (int jj = 0; jj < kChunkN; ++jj) {
+                    const int64_t n = n_first + kChunkCols * c + kChunkN * ns + jj;
                     if (n >= N || mvalid == 0) continue;
                     const int64_t idx = tl.pbase + n * M + mrow;
                     float* w = ch.w + 4 * jj;
@@ -422,8 +458,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, 
 
         auto process = [&](int c, Chunk& ch) {
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int64_t n = n_first + 16 * c + 4 * ns + jj;
+            for (int jj = 0; jj < kChunkN; ++jj) {
+                const int64_t n = n_first + kChunkCols * c + kChunkN * ns + jj;
                 if (n >= N || mvalid == 0) continue;
                 const int64_t idx = tl.pbase + n * M + mrow;
                 float* g = ch.g + 4 * jj;
@@ -486,10 +522,10 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, 
 __device__ __forceinline__ bool grouped_setup(const Params& p, int32_t* s_offs, int32_t* s_order,
                                               volatile int* s_bad)
 {
-    for (int i = threadIdx.x; i <= p.E; i += kThreads) s_offs[i] = p.offsets[i];
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_offs[i] = p.offsets[i];
     if (threadIdx.x == 0) *s_bad = 0;
     __syncthreads();
-    for (int e = threadIdx.x; e < p.E; e += kThreads) {
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
         const int32_t a = s_offs[e], b = s_offs[e + 1];
         if (a < 0 || b < a || static_cast<int64_t>(b) > p.T_max) *s_bad = 1;
     }
@@ -499,7 +535,7 @@ __device__ __forceinline__ bool grouped_setup(const Params& p, int32_t* s_offs, 
             *reinterpret_cast<volatile int*>(p.status) = kDevInvalidArg;
         return false;
     }
-    for (int e = threadIdx.x; e < p.E; e += kThreads) {
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
         const int32_t ke = s_offs[e + 1] - s_offs[e];
         int32_t rank = 0;
         for (int f = 0; f < p.E; ++f) {
@@ -588,7 +624,7 @@ __device__ __forceinline__ void load_block_cp_async(uint8_t* stage, const uint8_
 // ------------------------------------------------------------------ kernel
 
 template <int IT, int OP, int ST, bool GROUPED, bool MANUAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(EpiFor<GROUPED>::threads, 1)
     forge_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,   // dY
                        const __grid_constant__ CUtensorMap tmB,   // X
                        const __grid_constant__ CUtensorMap tmA1,  // dY, one-row boxes (grouped)
@@ -629,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&tfull[b], 1);
-            ptx::mbar_init(&tempty[b], kEpiWarps);
+            ptx::mbar_init(&tempty[b], EpiFor<GROUPED>::warps);
         }
         ptx::mbar_init(drain, 1);
         *abort_flag = 0;
@@ -857,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (; npend > 0; --npend) ptx::mbar_arrive(&full[(s - npend + kStages) % kStages]);
         }
     } else if (warp >= kEpiWarp0) {
-        epilogue_role<IT, OP, ST>(p, sc, smem, tfull, tmem_base, abort_flag, warp, lane,
+        epilogue_role<IT, OP, ST, EpiFor<GROUPED>>(p, sc, smem, tfull, tmem_base, abort_flag, warp, lane,
                                   [&](uint32_t b) { ptx::mbar_arrive(&tempty[b]); });
     }
 
@@ -902,7 +938,7 @@ constexpr int kPairStageBytes = kPairStageA + kPairStageB;
 static_assert(kPairStages * kPairStageBytes <= kSmemBarOffset, "pair ring fits the stage area");
 
 template <int IT, int OP, int ST, int NPAIR, bool GROUPED>
-__global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUPED>::threads, 1)
     forge_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,   // dY
                             const __grid_constant__ CUtensorMap tmB,   // X, boxes of BK / NPAIR rows
                             const __grid_constant__ CUtensorMap tmA1,  // dY, one-row boxes (grouped)
@@ -954,7 +990,7 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&tfull[b], 1);
-            ptx::mbar_init(&tempty[b], 2 * kEpiWarps);
+            ptx::mbar_init(&tempty[b], 2 * EpiFor<GROUPED>::warps);
         }
         ptx::mbar_init(drain, 1);
         *abort_flag = 0;
@@ -1127,7 +1163,7 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kEpiWarp0) {
         const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), lead_rank);
-        epilogue_role<IT, OP, ST>(p, sc, smem, tfull, tmem_base, abort_flag, warp, lane,
+        epilogue_role<IT, OP, ST, EpiFor<GROUPED>>(p, sc, smem, tfull, tmem_base, abort_flag, warp, lane,
                                   [&](uint32_t b) {
                                       if (leader)
                                           ptx::mbar_arrive(&tempty[b]);

@@ -44,7 +44,7 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
             if (e != cudaSuccess) return e;                                                    \
             cudaLaunchConfig_t cfg = {};                                                       \
             cfg.gridDim = dim3(2 * NPAIR, 1, 1);                                               \
-            cfg.blockDim = dim3(kThreads, 1, 1);                                               \
+            cfg.blockDim = dim3(EpiFor<GROUPED>::threads, 1, 1);                                               \
             cfg.dynamicSmemBytes = kSmemAlloc;                                                 \
             int n = 0;                                                                         \
             e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);                                \
@@ -53,7 +53,8 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
             __atomic_store_n(&mc, n, __ATOMIC_RELEASE);                                        \
         }                                                                                      \
         const int64_t nc = total_tiles < mc ? total_tiles : mc;                                \
-        kern<<<static_cast<int>(2 * NPAIR * nc), kThreads, kSmemAlloc, stream>>>(              \
+        kern<<<static_cast<int>(2 * NPAIR * nc), EpiFor<GROUPED>::threads, kSmemAlloc,         \
+               stream>>>(                                                                      \
             tmA, tmB, tmA1, tmB1, p);                                                          \
         return cudaGetLastError();                                                             \
     }                                                                                          \
@@ -83,7 +84,8 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
             if (e != cudaSuccess) return e;                                                    \
             __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);                              \
         }                                                                                      \
-        kern<<<grid, kThreads, kSmemAlloc, stream>>>(tmA, tmB, tmA1, tmB1, p);                 \
+        kern<<<grid, EpiFor<GROUPED>::threads, kSmemAlloc, stream>>>(tmA, tmB, tmA1, tmB1,     \
+                                                                     p);                       \
         return cudaGetLastError();                                                             \
     }                                                                                          \
     }
