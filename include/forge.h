@@ -35,9 +35,16 @@
  * An nn.Linear weight [d_out, d_in] is the transpose of W; pass it as its
  * [d_in, d_out] row-major view.
  *
- * Ownership and ordering: every pointer is caller-owned device memory.  The
- * library allocates nothing per call and keeps no pointer after the call
- * returns.  W, m, v, buf are updated in place.  Calls are asynchronous and
+ * Ownership and ordering: every pointer is caller-owned device memory and
+ * the library keeps no pointer after the call returns.  It allocates nothing
+ * per call, with one exception: an operand (X or dY) whose base is not
+ * 16-byte aligned or whose row stride is not a multiple of 16 bytes is first
+ * copied into a padded scratch buffer taken from the device's default memory
+ * pool with cudaMallocAsync on `stream` and returned with cudaFreeAsync on
+ * the same stream after the kernel (one extra read and write of that
+ * operand).  If that allocation fails, or the environment variable
+ * FORGE_MISALIGNED is "loader", the kernel fetches such an operand itself
+ * with cp.async instead.  W, m, v, buf are updated in place.  Calls are asynchronous and
  * ordered on `stream`; the return value reports only host-side validation
  * and launch errors.  Errors detected on the device (a bounded wait that
  * ran out) are recorded in a device status word read by
@@ -53,8 +60,9 @@
  * Host-side checks run before any CUDA call, in this order: null pointers
  * (X and dY may be NULL only when K == 0), sizes (M >= 1, N >= 1, K >= 0,
  * E >= 1, step >= 1), dtypes, then the device (compute capability 10.3),
- * then alignment (16-byte aligned bases of X, dY; 4-byte of W, m, v, dW;
- * see FORGE_ERR_MISALIGNED).
+ * then alignment (X, dY: base and row stride multiples of 4 bytes, of 16
+ * bytes to be read by TMA without staging; W, dW: 4-byte bases; m, v, buf:
+ * bases aligned to their element size; see FORGE_ERR_MISALIGNED).
  */
 #ifndef FORGE_H
 #define FORGE_H

@@ -69,6 +69,14 @@ def scales_dev(sc, dev):
     return torch.tensor(sc, dtype=torch.float32, device=dev)
 
 
+@pytest.fixture(params=["stage", "loader"])
+def misaligned_path(request, monkeypatch):
+    """Operands TMA cannot address: staged into a padded copy, or fetched by
+    the kernel's cp.async loader."""
+    monkeypatch.setenv("FORGE_MISALIGNED", request.param)
+    return request.param
+
+
 @pytest.fixture(params=["single", "pair", "quad"])
 def kernel_form(request, monkeypatch):
     """Run a dense test on the one-CTA kernel, on CTA pairs and on two-pair clusters."""
@@ -381,8 +389,9 @@ def test_grouped_bad_offsets_flagged_on_device(cuda_device):
 
 # ------------------------------------------------------------------ rows TMA cannot address
 
-# (K, N, M): row strides that are not multiples of 16 bytes go through the
-# cp.async loader; d_out not a multiple of 4 also exercises the scalar epilogue
+# (K, N, M): row strides that are not multiples of 16 bytes are staged into a
+# padded copy for TMA or fetched by the cp.async loader; d_out not a multiple
+# of 4 also exercises the scalar epilogue
 SHAPES_MISALIGNED_BF16 = [
     (300, 264, 4100),   # dY rows 8200 B -> 8-byte copies
     (130, 264, 302),    # dY rows 604 B -> 4-byte copies, scalar epilogue
@@ -393,7 +402,7 @@ SHAPES_MISALIGNED_BF16 = [
 
 
 @pytest.mark.parametrize("K,N,M", SHAPES_MISALIGNED_BF16)
-def test_wgrad_only_misaligned_rows(cuda_device, K, N, M):
+def test_wgrad_only_misaligned_rows(cuda_device, misaligned_path, K, N, M):
     X, D = bf16_inputs(K, N, M, 40)
     dW = torch.full((N, M), float("nan"), device=cuda_device)
     fg.forge_wgrad_only(X.to(cuda_device), D.to(cuda_device), dW)
@@ -403,7 +412,7 @@ def test_wgrad_only_misaligned_rows(cuda_device, K, N, M):
 
 @pytest.mark.parametrize("state_bf16", [False, True], ids=["f32state", "bf16state"])
 @pytest.mark.parametrize("K,N,M", SHAPES_MISALIGNED_BF16)
-def test_adamw_misaligned_rows(cuda_device, K, N, M, state_bf16):
+def test_adamw_misaligned_rows(cuda_device, misaligned_path, K, N, M, state_bf16):
     X, D = bf16_inputs(K, N, M, 41)
     W, m, v = warm_state(N, M, 42, state_bf16)
     got = run_adamw(cuda_device, X, D, W, m, v, step=5)
@@ -413,7 +422,7 @@ def test_adamw_misaligned_rows(cuda_device, K, N, M, state_bf16):
 
 
 @pytest.mark.parametrize("K,N,M", [(256, 520, 1000), (100, 260, 4100)])
-def test_e4m3_misaligned_rows(cuda_device, K, N, M):
+def test_e4m3_misaligned_rows(cuda_device, misaligned_path, K, N, M):
     X, D, sc = e4m3_inputs(K, N, M, 43)
     W, m, v = warm_state(N, M, 44)
     got = run_adamw(cuda_device, X, D, W, m, v, step=2, scales=sc)
@@ -422,7 +431,7 @@ def test_e4m3_misaligned_rows(cuda_device, K, N, M):
     check_adamw(got, ref, G, HP.lr, False)
 
 
-def test_offset_base_pointers(cuda_device):
+def test_offset_base_pointers(cuda_device, misaligned_path):
     # operands that start 8 bytes into an allocation: TMA needs 16-byte bases
     K, N, M = 96, 264, 136
     X, D = bf16_inputs(K, N, M, 45)
@@ -438,7 +447,7 @@ def test_offset_base_pointers(cuda_device):
     check_dw(dW.cpu().numpy(), oracle.wgrad(X, D))
 
 
-def test_grouped_misaligned_rows(cuda_device, grouped_form):
+def test_grouped_misaligned_rows(cuda_device, misaligned_path, grouped_form):
     counts = [37, 0, 100, 9]
     N, M = 264, 4100
     X, D, off, W, m, v, sc = grouped_case(counts, N, M, 46)

@@ -2,10 +2,11 @@
 // checks, TMA descriptor encoding, tile-grid sizing and kernel dispatch.
 //
 // Every check on the arguments runs before the first CUDA call, so invalid
-// calls fail with a status code even on a machine without a GPU.  The
-// library keeps no per-call allocation: the only device memory it owns is
-// the status word below, which exists once per device for the life of the
-// process.
+// calls fail with a status code even on a machine without a GPU.  The only
+// device memory the library owns for the life of the process is the status
+// word below (once per device); the one per-call allocation is the staging
+// copy of an operand whose rows TMA cannot address (stream-ordered, freed on
+// the same stream after the kernel).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -95,11 +96,12 @@ forge_status current_device(DeviceInfo** out)
     return FORGE_OK;
 }
 
-// 2-D token-major operand [rows, inner] -> TMA map with 128-byte swizzled
-// boxes of (128 bytes of the inner dimension) x (k rows per stage / row_split).
-// row_split = 0 asks for one-row boxes, the form tile::gather4 copies use.
+// 2-D token-major operand [rows, inner] with a row stride of ld_bytes (a
+// multiple of 16) -> TMA map with 128-byte swizzled boxes of (128 bytes of
+// the inner dimension) x (k rows per stage / row_split).  row_split = 0 asks
+// for one-row boxes, the form tile::gather4 copies use.
 forge_status encode_operand(CUtensorMap* map, const void* base, forge_dtype dt, int64_t inner,
-                            int64_t rows, int row_split = 1)
+                            int64_t rows, int64_t ld_bytes, int row_split = 1)
 {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
@@ -119,7 +121,7 @@ forge_status encode_operand(CUtensorMap* map, const void* base, forge_dtype dt, 
                        : (dt == FORGE_BF16 ? InTraits<IN_BF16>::BK : InTraits<IN_E4M3>::BK) /
                              row_split;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * es};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_bytes)};
     cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType t =
@@ -150,6 +152,63 @@ __global__ void forge_wait_selftest_kernel(int64_t timeout_ns, int* status)
 }
 
 forge_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FORGE_OK : FORGE_ERR_CUDA; }
+
+// ------------------------------------------------------------------ operand staging
+
+// Copies `rows` rows of `units` U-sized units (source rows packed, `units`
+// apart) into rows `dst_units` apart, leaving the padding at the end of each
+// destination row unwritten (the tensor map's extent stops before it).  A
+// block walks whole rows; each thread keeps four loads in flight.
+template <typename U>
+__global__ void __launch_bounds__(256) forge_stage_rows_kernel(const U* __restrict__ src,
+                                                               U* __restrict__ dst, int64_t rows,
+                                                               int64_t units, int64_t dst_units)
+{
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const U* s = src + r * units;
+        U* d = dst + r * dst_units;
+        for (int64_t u0 = threadIdx.x; u0 < units; u0 += 4 * blockDim.x) {
+            U v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t u = u0 + j * blockDim.x;
+                if (u < units) v[j] = __ldcs(s + u);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t u = u0 + j * blockDim.x;
+                if (u < units) d[u] = v[j];
+            }
+        }
+    }
+}
+
+// Stages [rows, row_bytes] (base and stride aligned to `gran` = 8 or 4
+// bytes) into dst with a row stride of dst_row_bytes (a multiple of 16).
+cudaError_t stage_rows(const void* src, void* dst, int64_t rows, int64_t row_bytes,
+                       int64_t dst_row_bytes, int gran, int sms, cudaStream_t stream)
+{
+    const int64_t blocks64 = rows < 8LL * sms ? rows : 8LL * sms;
+    const int blocks = static_cast<int>(blocks64 > 0 ? blocks64 : 1);
+    if (gran == 8)
+        forge_stage_rows_kernel<uint2><<<blocks, 256, 0, stream>>>(
+            static_cast<const uint2*>(src), static_cast<uint2*>(dst), rows, row_bytes / 8,
+            dst_row_bytes / 8);
+    else
+        forge_stage_rows_kernel<uint32_t><<<blocks, 256, 0, stream>>>(
+            static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), rows, row_bytes / 4,
+            dst_row_bytes / 4);
+    return cudaGetLastError();
+}
+
+// Operands whose rows TMA cannot address are either staged into a padded
+// copy (default) or fetched by the kernel's cp.async loader.
+// FORGE_MISALIGNED = loader | stage (read on every call) overrides.
+bool stage_misaligned()
+{
+    const char* e = std::getenv("FORGE_MISALIGNED");
+    return !(e && std::strcmp(e, "loader") == 0);
+}
 
 // The four operand maps of one call: dY and X with whole k-block boxes, and
 // (grouped calls) the same tensors with one-row boxes for gathered blocks.
@@ -268,30 +327,71 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
                    ? 1
                    : 0;
 
+    // Operands TMA cannot address: a padded staging copy with 16-byte rows
+    // (one HBM-bound pass, then the TMA kernels), unless the caller asks for
+    // the in-kernel loader or the allocation fails.
+    const void* opA = dY;
+    const void* opB = X;
+    int64_t ldA = p.M * es, ldB = p.N * es;
+    void* scratch = nullptr;
+    if (rows > 0 && (p.manual_a || p.manual_b) && stage_misaligned()) {
+        const int64_t pa = p.manual_a ? (ldA + 15) / 16 * 16 : 0;
+        const int64_t pb = p.manual_b ? (ldB + 15) / 16 * 16 : 0;
+        if (cudaMallocAsync(&scratch, static_cast<size_t>((pa + pb) * rows), stream) ==
+            cudaSuccess) {
+            uint8_t* sp = static_cast<uint8_t*>(scratch);
+            cudaError_t ce = cudaSuccess;
+            if (p.manual_a) {
+                ce = stage_rows(dY, sp, rows, ldA, pa, p.gran_a, dev->sms, stream);
+                opA = sp;
+                ldA = pa;
+                p.manual_a = 0;
+                sp += pa * rows;
+            }
+            if (ce == cudaSuccess && p.manual_b) {
+                ce = stage_rows(X, sp, rows, ldB, pb, p.gran_b, dev->sms, stream);
+                opB = sp;
+                ldB = pb;
+                p.manual_b = 0;
+            }
+            if (ce != cudaSuccess) {
+                cudaFreeAsync(scratch, stream);
+                return FORGE_ERR_CUDA;
+            }
+        } else {
+            cudaGetLastError();
+            scratch = nullptr;
+        }
+    }
+
     const bool man = p.manual_a || p.manual_b;
     const int form = kernel_form(p, grouped, man);
     Maps maps;
     std::memset(&maps, 0, sizeof maps);
     p.has_maps = rows > 0 ? 1 : 0;
     if (rows > 0) {
-        if (!p.manual_a && (st = encode_operand(&maps.a, dY, in_dtype, p.M, rows)) != FORGE_OK)
-            return st;
+        st = FORGE_OK;
+        if (!p.manual_a) st = encode_operand(&maps.a, opA, in_dtype, p.M, rows, ldA);
         // two pairs fetch half of each X box's k rows apiece
-        if (!p.manual_b && (st = encode_operand(&maps.b, X, in_dtype, p.N, rows,
-                                                form == 2 ? 2 : 1)) != FORGE_OK)
+        if (st == FORGE_OK && !p.manual_b)
+            st = encode_operand(&maps.b, opB, in_dtype, p.N, rows, ldB, form == 2 ? 2 : 1);
+        if (st == FORGE_OK && grouped && !p.manual_a)
+            st = encode_operand(&maps.a1, opA, in_dtype, p.M, rows, ldA, 0);
+        if (st == FORGE_OK && grouped && !p.manual_b)
+            st = encode_operand(&maps.b1, opB, in_dtype, p.N, rows, ldB, 0);
+        if (st != FORGE_OK) {
+            if (scratch) cudaFreeAsync(scratch, stream);
             return st;
-        if (grouped && !p.manual_a &&
-            (st = encode_operand(&maps.a1, dY, in_dtype, p.M, rows, 0)) != FORGE_OK)
-            return st;
-        if (grouped && !p.manual_b &&
-            (st = encode_operand(&maps.b1, X, in_dtype, p.N, rows, 0)) != FORGE_OK)
-            return st;
+        }
     }
     const int64_t tile_m = form == 2 ? 4 * BM : (form == 1 ? 2 * BM : BM);
     const int64_t tiles_m = (p.M + tile_m - 1) / tile_m;
     const int64_t tiles_n = (p.N + BN - 1) / BN;
     const int64_t total = tiles_m * tiles_n * p.E;
-    if (total <= 0 || total > INT32_MAX) return FORGE_ERR_INVALID_ARG;
+    if (total <= 0 || total > INT32_MAX) {
+        if (scratch) cudaFreeAsync(scratch, stream);
+        return FORGE_ERR_INVALID_ARG;
+    }
     p.tiles_m = static_cast<int32_t>(tiles_m);
     p.tiles_n = static_cast<int32_t>(tiles_n);
     p.raster_band = raster_band(p.tiles_m);
@@ -310,15 +410,20 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
             e = in_dtype == FORGE_BF16
                     ? dispatch_pair<IN_BF16, 2>(op, ist, false, maps, p, total, stream)
                     : dispatch_pair<IN_E4M3, 2>(op, ist, false, maps, p, total, stream);
-        return from_cuda(e);
+    } else {
+        const int grid = static_cast<int>(total < dev->sms ? total : dev->sms);
+        if (in_dtype == FORGE_BF16)
+            e = man ? dispatch_op<IN_BF16, true>(op, ist, grouped, maps, p, grid, stream)
+                    : dispatch_op<IN_BF16, false>(op, ist, grouped, maps, p, grid, stream);
+        else
+            e = man ? dispatch_op<IN_E4M3, true>(op, ist, grouped, maps, p, grid, stream)
+                    : dispatch_op<IN_E4M3, false>(op, ist, grouped, maps, p, grid, stream);
     }
-    const int grid = static_cast<int>(total < dev->sms ? total : dev->sms);
-    if (in_dtype == FORGE_BF16)
-        e = man ? dispatch_op<IN_BF16, true>(op, ist, grouped, maps, p, grid, stream)
-                : dispatch_op<IN_BF16, false>(op, ist, grouped, maps, p, grid, stream);
-    else
-        e = man ? dispatch_op<IN_E4M3, true>(op, ist, grouped, maps, p, grid, stream)
-                : dispatch_op<IN_E4M3, false>(op, ist, grouped, maps, p, grid, stream);
+    // the staging copy is released after the kernel, in stream order
+    if (scratch) {
+        const cudaError_t fe = cudaFreeAsync(scratch, stream);
+        if (e == cudaSuccess) e = fe;
+    }
     return from_cuda(e);
 }
 
