@@ -89,7 +89,8 @@ typedef enum {
     FORGE_ERR_UNSUPPORTED_DEVICE = -3,/* no device, or compute capability != 10.3 */
     FORGE_ERR_MISALIGNED = -4,        /* a base pointer or row stride the kernels cannot address */
     FORGE_ERR_CUDA = -5,              /* a CUDA runtime / driver call failed */
-    FORGE_ERR_TIMEOUT = -6            /* a device-side bounded wait ran out */
+    FORGE_ERR_TIMEOUT = -6,           /* a device-side bounded wait ran out */
+    FORGE_ERR_SCRATCH_TOO_SMALL = -7  /* forge_wgrad_adamw_noalloc: staging exceeds its buffer */
 } forge_status;
 
 typedef enum {
@@ -119,6 +120,41 @@ FORGE_API forge_status forge_wgrad_adamw(const void* X, const void* dY, float* W
                                forge_dtype state_dtype, float lr, float beta1, float beta2,
                                float eps, float wd, int64_t step, const float* scales,
                                forge_stream_t stream);
+
+/*
+ * forge_wgrad_adamw without any device allocation.  The FORGE pages have no
+ * counterpart to this call: it is a library variant of forge_wgrad_adamw for
+ * callers that must not allocate device memory during a step.  Arguments,
+ * layouts, checks and results are those of forge_wgrad_adamw (the results
+ * are bitwise identical); only the staging copy of an operand whose base or
+ * row stride is not 16-byte aligned differs: it goes into a fixed 256 MiB
+ * buffer per device, a file-scope device array inside the library, instead
+ * of a stream-ordered allocation.
+ *   - Oversize: a call whose staging copy needs more than the buffer
+ *     ((rows of X, dY) x (row bytes rounded up to 16), summed over the
+ *     operands that need staging) returns FORGE_ERR_SCRATCH_TOO_SMALL before
+ *     any launch and changes nothing.  Aligned operands need no staging.
+ *   - Races: the buffer is shared by every call of this function on the
+ *     device.  Calls that stage must be ordered (one stream, or streams
+ *     synchronised with each other); two overlapping calls on unordered
+ *     streams overwrite each other's staging copy.  forge_wgrad_adamw and
+ *     the other entry points never touch the buffer.
+ *   - State: each call writes every byte of the buffer that its kernel then
+ *     reads (the padding after each staged row lies outside the tensor maps),
+ *     so nothing carries over from an earlier call.
+ *   - First-call setup: the first call on a device resolves the buffer's
+ *     address (cudaGetSymbolAddress), which loads the library module holding
+ *     it and reserves its 256 MiB there for the life of the process.  Make
+ *     that first call outside stream capture; later calls are capturable.
+ *   - FORGE_MISALIGNED=loader selects the kernel's own cp.async loader here
+ *     too (no staging, no buffer).
+ */
+FORGE_API forge_status forge_wgrad_adamw_noalloc(const void* X, const void* dY, float* W, void* m,
+                                                 void* v, int64_t M, int64_t N, int64_t K,
+                                                 forge_dtype in_dtype, forge_dtype state_dtype,
+                                                 float lr, float beta1, float beta2, float eps,
+                                                 float wd, int64_t step, const float* scales,
+                                                 forge_stream_t stream);
 
 /*
  * Fused dW = X^T dY and one SGD-momentum step on W and the momentum buffer

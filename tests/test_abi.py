@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for code in range(-6, 1):
+    for code in range(-7, 1):
         s = fg.forge_status_string(code)
         assert isinstance(s, str) and s and s != "unknown status"
     assert fg.forge_status_string(-99) == "unknown status"
@@ -58,8 +58,8 @@ HP = (1e-3, 0.9, 0.999, 1e-8, 0.01)
 
 
 def adamw(L, X=FAKE, dY=FAKE, W=FAKE, m=FAKE, v=FAKE, M=64, N=64, K=64, it=fg.FORGE_BF16,
-          st=fg.FORGE_F32, hp=HP, step=1, scales=None):
-    return L.forge_wgrad_adamw(X, dY, W, m, v, M, N, K, it, st, *hp, step, scales, None)
+          st=fg.FORGE_F32, hp=HP, step=1, scales=None, fn="forge_wgrad_adamw"):
+    return getattr(L, fn)(X, dY, W, m, v, M, N, K, it, st, *hp, step, scales, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -84,8 +84,9 @@ def adamw(L, X=FAKE, dY=FAKE, W=FAKE, m=FAKE, v=FAKE, M=64, N=64, K=64, it=fg.FO
     (dict(hp=(1e-3, 0.9, 0.999, -1.0, 0.01)), fg.FORGE_ERR_INVALID_ARG),
     (dict(hp=(1e-3, 0.9, 0.999, 1e-8, float("inf"))), fg.FORGE_ERR_INVALID_ARG),
 ])
-def test_adamw_rejects_invalid_arguments(L, kw, code):
-    assert adamw(L, **kw) == code
+@pytest.mark.parametrize("fn", ["forge_wgrad_adamw", "forge_wgrad_adamw_noalloc"])
+def test_adamw_rejects_invalid_arguments(L, kw, code, fn):
+    assert adamw(L, fn=fn, **kw) == code
 
 
 def test_sgdm_and_wgrad_only_reject_invalid_arguments(L):
@@ -121,4 +122,5 @@ def test_valid_call_without_gpu_fails_closed(L):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present; the fake pointers must not reach a kernel")
     assert adamw(L) == fg.FORGE_ERR_UNSUPPORTED_DEVICE
+    assert adamw(L, fn="forge_wgrad_adamw_noalloc") == fg.FORGE_ERR_UNSUPPORTED_DEVICE
     assert fg.forge_get_device_status() == fg.FORGE_ERR_UNSUPPORTED_DEVICE

@@ -1,0 +1,83 @@
+"""GPU tests of forge_wgrad_adamw_noalloc, the entry point that stages
+misaligned operands into the library's fixed per-device buffer instead of
+allocating.  Its results must equal forge_wgrad_adamw's bit for bit, call
+after call, and a call whose staging copy would not fit must be refused
+before anything is written."""
+import numpy as np
+import pytest
+import torch
+
+import weight_grad_gemm_gb300 as fg
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.01)
+
+
+def state(N, M, seed, dev):
+    W = wl.randn((N, M), wl.seed_of("na-W", seed), device=dev, std=0.02)
+    m = wl.randn((N, M), wl.seed_of("na-m", seed), device=dev, std=1e-3)
+    v = wl.randn((N, M), wl.seed_of("na-v", seed), device=dev, std=1e-3) ** 2
+    return W, m, v
+
+
+def bits(t):
+    return t.view(torch.int32).cpu().numpy()
+
+
+def test_no_alloc_matches_allocating_entry_call_after_call(cuda_device, monkeypatch):
+    """Consecutive calls on two layers whose X rows (1044 bytes) and dY rows
+    (8200, then 2004 bytes) both need staging: each call overwrites part of
+    what the previous one left in the buffer with another layout, and layer
+    a's second step starts from the state its first step wrote."""
+    monkeypatch.delenv("FORGE_MISALIGNED", raising=False)
+    dev = cuda_device
+    layers = {"a": (522, 4100), "b": (522, 1002)}
+    ref = {k: state(N, M, i, dev) for i, (k, (N, M)) in enumerate(layers.items())}
+    got = {k: tuple(t.clone() for t in ref[k]) for k in layers}
+    for step, name, K in ((1, "a", 300), (1, "b", 200), (2, "a", 300)):
+        N, M = layers[name]
+        X = wl.activations(K, N, wl.seed_of("na-X", name, step), device=dev)
+        D = wl.activations(K, M, wl.seed_of("na-dY", name, step), device=dev)
+        fg.forge_wgrad_adamw(X, D, *ref[name], step=step, **HP)
+        fg.forge_wgrad_adamw_noalloc(X, D, *got[name], step=step, **HP)
+        torch.cuda.synchronize()
+        assert fg.forge_get_device_status() == fg.FORGE_OK
+        for a, b in zip(ref[name], got[name]):
+            assert np.array_equal(bits(a), bits(b))
+        assert torch.isfinite(got[name][0]).all()
+
+
+def test_no_alloc_aligned_operands_match(cuda_device):
+    dev = cuda_device
+    K, N, M = 256, 520, 264
+    X = wl.activations(K, N, wl.seed_of("na-X", 9), device=dev)
+    D = wl.activations(K, M, wl.seed_of("na-dY", 9), device=dev)
+    W1, m1, v1 = state(N, M, 9, dev)
+    W2, m2, v2 = W1.clone(), m1.clone(), v1.clone()
+    fg.forge_wgrad_adamw(X, D, W1, m1, v1, step=3, **HP)
+    fg.forge_wgrad_adamw_noalloc(X, D, W2, m2, v2, step=3, **HP)
+    torch.cuda.synchronize()
+    for a, b in ((W1, W2), (m1, m2), (v1, v2)):
+        assert np.array_equal(bits(a), bits(b))
+
+
+def test_no_alloc_refuses_staging_larger_than_its_buffer(cuda_device, monkeypatch):
+    """33000 rows of 8200 bytes need 33000 x 8208 bytes > 256 MiB of staging."""
+    monkeypatch.delenv("FORGE_MISALIGNED", raising=False)
+    dev = cuda_device
+    K, N, M = 33000, 8, 4100
+    X = torch.zeros((K, N), dtype=torch.bfloat16, device=dev)
+    D = torch.zeros((K, M), dtype=torch.bfloat16, device=dev)
+    W, m, v = state(N, M, 3, dev)
+    W0 = W.clone()
+    with pytest.raises(fg.ForgeError) as e:
+        fg.forge_wgrad_adamw_noalloc(X, D, W, m, v, step=1, **HP)
+    assert e.value.status == fg.FORGE_ERR_SCRATCH_TOO_SMALL
+    torch.cuda.synchronize()
+    assert torch.equal(W, W0)
+    # the allocating entry point takes the same call
+    fg.forge_wgrad_adamw(X, D, W, m, v, step=1, **HP)
+    torch.cuda.synchronize()
+    assert fg.forge_get_device_status() == fg.FORGE_OK

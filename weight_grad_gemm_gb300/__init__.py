@@ -27,12 +27,13 @@ FORGE_ERR_UNSUPPORTED_DEVICE = -3
 FORGE_ERR_MISALIGNED = -4
 FORGE_ERR_CUDA = -5
 FORGE_ERR_TIMEOUT = -6
+FORGE_ERR_SCRATCH_TOO_SMALL = -7
 
 FORGE_BF16 = 0
 FORGE_E4M3 = 1
 FORGE_F32 = 2
 
-EXPORTS = ("forge_wgrad_adamw", "forge_wgrad_sgdm", "forge_wgrad_only",
+EXPORTS = ("forge_wgrad_adamw", "forge_wgrad_adamw_noalloc", "forge_wgrad_sgdm", "forge_wgrad_only",
            "forge_grouped_wgrad_adamw", "forge_status_string", "forge_get_device_status",
            "forge_selftest_wait_timeout", "forge_version")
 
@@ -57,11 +58,13 @@ def lib() -> ctypes.CDLL:
     P, I64, I32, F, I = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
                          ctypes.c_int)
     L.forge_wgrad_adamw.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, F, F, F, F, F, I64, P, P]
+    L.forge_wgrad_adamw_noalloc.argtypes = L.forge_wgrad_adamw.argtypes
     L.forge_wgrad_sgdm.argtypes = [P, P, P, P, I64, I64, I64, I, I, F, F, F, P, P]
     L.forge_wgrad_only.argtypes = [P, P, P, I64, I64, I64, I, P, P]
     L.forge_grouped_wgrad_adamw.argtypes = [P, P, P, P, P, P, I32, I64, I64, I64, I, I, F, F, F,
                                             F, F, I64, P, P]
-    for f in ("forge_wgrad_adamw", "forge_wgrad_sgdm", "forge_wgrad_only",
+    for f in ("forge_wgrad_adamw", "forge_wgrad_adamw_noalloc", "forge_wgrad_sgdm",
+              "forge_wgrad_only",
               "forge_grouped_wgrad_adamw", "forge_get_device_status",
               "forge_selftest_wait_timeout"):
         getattr(L, f).restype = I
@@ -127,18 +130,31 @@ def _scales_ptr(scales, X):
 
 # ---- the C ABI, tensor form ------------------------------------------------
 
-def forge_wgrad_adamw(X, dY, W, m, v, *, lr, beta1, beta2, eps, wd, step, scales=None,
-                      stream=None):
+def _adamw_call(name, X, dY, W, m, v, lr, beta1, beta2, eps, wd, step, scales, stream):
     M, N, K = _sizes(X, dY)
     for t in (W, m, v):
         if tuple(t.shape) != (N, M):
             raise ValueError(f"W/m/v must be [N={N}, M={M}], got {tuple(t.shape)}")
     if m.dtype != v.dtype:
         raise TypeError("m and v must share a dtype")
-    s = lib().forge_wgrad_adamw(_ptr(X), _ptr(dY), _ptr(W), _ptr(m), _ptr(v), M, N, K,
-                                _dtype_code(X), _dtype_code(m), lr, beta1, beta2, eps, wd,
-                                int(step), _scales_ptr(scales, X), _stream(stream, W))
-    _check(s, "forge_wgrad_adamw")
+    s = getattr(lib(), name)(_ptr(X), _ptr(dY), _ptr(W), _ptr(m), _ptr(v), M, N, K,
+                             _dtype_code(X), _dtype_code(m), lr, beta1, beta2, eps, wd,
+                             int(step), _scales_ptr(scales, X), _stream(stream, W))
+    _check(s, name)
+
+
+def forge_wgrad_adamw(X, dY, W, m, v, *, lr, beta1, beta2, eps, wd, step, scales=None,
+                      stream=None):
+    _adamw_call("forge_wgrad_adamw", X, dY, W, m, v, lr, beta1, beta2, eps, wd, step, scales,
+                stream)
+
+
+def forge_wgrad_adamw_noalloc(X, dY, W, m, v, *, lr, beta1, beta2, eps, wd, step, scales=None,
+                              stream=None):
+    """forge_wgrad_adamw staging misaligned operands into the library's fixed
+    per-device buffer instead of allocating (see include/forge.h)."""
+    _adamw_call("forge_wgrad_adamw_noalloc", X, dY, W, m, v, lr, beta1, beta2, eps, wd, step,
+                scales, stream)
 
 
 def forge_wgrad_sgdm(X, dY, W, mom, *, lr, momentum, wd, scales=None, stream=None):

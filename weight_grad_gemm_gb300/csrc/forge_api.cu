@@ -2,11 +2,12 @@
 // checks, TMA descriptor encoding, tile-grid sizing and kernel dispatch.
 //
 // Every check on the arguments runs before the first CUDA call, so invalid
-// calls fail with a status code even on a machine without a GPU.  The only
-// device memory the library owns for the life of the process is the status
-// word below (once per device); the one per-call allocation is the staging
-// copy of an operand whose rows TMA cannot address (stream-ordered, freed on
-// the same stream after the kernel).
+// calls fail with a status code even on a machine without a GPU.  The device
+// memory the library owns for the life of the process is the status word
+// below (once per device) and, once forge_wgrad_adamw_noalloc has run on a
+// device, its fixed staging buffer; the one per-call allocation is the
+// staging copy of an operand whose rows TMA cannot address (stream-ordered,
+// freed on the same stream after the kernel).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -19,6 +20,7 @@
 
 #include "forge.h"
 #include "forge_launch.cuh"
+#include "forge_static_stage.h"
 
 namespace {
 
@@ -293,10 +295,15 @@ int operand_path(const void* base, int64_t ld, int es)
     return -1;
 }
 
+// Where a staging copy lives: a stream-ordered allocation from the device's
+// default pool, or the fixed per-device buffer of the no-allocation entry.
+enum class StageFrom { Pool, Static };
+
 // Shared tail of every entry point, after the argument checks.
 //   rows: K (dense) or T_max (grouped) -- the rows of X and dY.
 forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dtype, int op,
-                 forge_dtype state_dtype, bool grouped, Params p, cudaStream_t stream)
+                 forge_dtype state_dtype, bool grouped, Params p, cudaStream_t stream,
+                 StageFrom stage_from = StageFrom::Pool)
 {
     DeviceInfo* dev = nullptr;
     forge_status st = current_device(&dev);
@@ -333,13 +340,29 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
     const void* opA = dY;
     const void* opB = X;
     int64_t ldA = p.M * es, ldB = p.N * es;
-    void* scratch = nullptr;
+    void* scratch = nullptr;  // pool allocation to return after the kernel
     if (rows > 0 && (p.manual_a || p.manual_b) && stage_misaligned()) {
         const int64_t pa = p.manual_a ? (ldA + 15) / 16 * 16 : 0;
         const int64_t pb = p.manual_b ? (ldB + 15) / 16 * 16 : 0;
-        if (cudaMallocAsync(&scratch, static_cast<size_t>((pa + pb) * rows), stream) ==
-            cudaSuccess) {
-            uint8_t* sp = static_cast<uint8_t*>(scratch);
+        const int64_t need = (pa + pb) * rows;
+        void* stage = nullptr;
+        if (stage_from == StageFrom::Static) {
+            // fixed buffer: refuse what does not fit, before any launch
+            if (need > static_cast<int64_t>(static_stage_capacity()))
+                return FORGE_ERR_SCRATCH_TOO_SMALL;
+            int d = 0;
+            if (cudaGetDevice(&d) != cudaSuccess || static_stage_address(d, &stage) != cudaSuccess) {
+                cudaGetLastError();
+                return FORGE_ERR_CUDA;
+            }
+        } else if (cudaMallocAsync(&scratch, static_cast<size_t>(need), stream) == cudaSuccess) {
+            stage = scratch;
+        } else {
+            cudaGetLastError();
+            scratch = nullptr;
+        }
+        if (stage) {
+            uint8_t* sp = static_cast<uint8_t*>(stage);
             cudaError_t ce = cudaSuccess;
             if (p.manual_a) {
                 ce = stage_rows(dY, sp, rows, ldA, pa, p.gran_a, dev->sms, stream);
@@ -355,12 +378,9 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
                 p.manual_b = 0;
             }
             if (ce != cudaSuccess) {
-                cudaFreeAsync(scratch, stream);
+                if (scratch) cudaFreeAsync(scratch, stream);
                 return FORGE_ERR_CUDA;
             }
-        } else {
-            cudaGetLastError();
-            scratch = nullptr;
         }
     }
 
@@ -498,6 +518,32 @@ forge_status forge_wgrad_adamw(const void* X, const void* dY, float* W, void* m,
                reinterpret_cast<cudaStream_t>(stream));
 }
 
+forge_status forge_wgrad_adamw_noalloc(const void* X, const void* dY, float* W, void* m, void* v,
+                                       int64_t M, int64_t N, int64_t K, forge_dtype in_dtype,
+                                       forge_dtype state_dtype, float lr, float beta1,
+                                       float beta2, float eps, float wd, int64_t step,
+                                       const float* scales, forge_stream_t stream)
+{
+    if (!W || !m || !v) return FORGE_ERR_INVALID_ARG;
+    forge_status s;
+    if ((s = check_sizes(M, N, K)) != FORGE_OK) return s;
+    if ((s = check_inputs(X, dY, K, in_dtype, scales)) != FORGE_OK) return s;
+    if (state_dtype != FORGE_F32 && state_dtype != FORGE_BF16) return FORGE_ERR_UNSUPPORTED_DTYPE;
+    if ((s = check_adam(lr, beta1, beta2, eps, wd, step)) != FORGE_OK) return s;
+    Params p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.E = 1;
+    p.W = W;
+    p.s1 = m;
+    p.s2 = v;
+    p.scales = scales;
+    fill_adam(p, lr, beta1, beta2, eps, wd, step);
+    return run(X, dY, K, in_dtype, OP_ADAMW, state_dtype, false, p,
+               reinterpret_cast<cudaStream_t>(stream), StageFrom::Static);
+}
+
 forge_status forge_wgrad_sgdm(const void* X, const void* dY, float* W, void* mom, int64_t M,
                               int64_t N, int64_t K, forge_dtype in_dtype, forge_dtype state_dtype,
                               float lr, float momentum, float wd, const float* scales,
@@ -586,6 +632,7 @@ const char* forge_status_string(forge_status status)
     case FORGE_ERR_MISALIGNED: return "misaligned pointer or row stride";
     case FORGE_ERR_CUDA: return "CUDA error";
     case FORGE_ERR_TIMEOUT: return "device-side wait timed out";
+    case FORGE_ERR_SCRATCH_TOO_SMALL: return "operand staging needs more than the fixed scratch buffer";
     }
     return "unknown status";
 }
