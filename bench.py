@@ -52,16 +52,21 @@ def load_peaks():
         return dict(PEAKS_FALLBACK), "fallback"
 
 
+# The sources the fused kernel and its launch are built from.
+FUSED_SOURCES = ("forge_api.cu", "forge_kernel.cuh", "forge_launch.cuh", "forge_ptx.cuh",
+                 "kernels_bf16.cu", "kernels_e4m3.cu", "kernels_pair_bf16.cu",
+                 "kernels_pair_e4m3.cu")
+
+
 def csrc_digest():
-    """sha256 over the CUDA sources (file name + content, sorted by name)."""
+    """sha256 over the fused kernel's sources (file name + content, sorted)."""
     import hashlib
     d = os.path.join(ROOT, "weight_grad_gemm_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(f.encode())
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+    for f in sorted(FUSED_SOURCES):
+        h.update(f.encode())
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()
 
 
