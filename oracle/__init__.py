@@ -68,6 +68,8 @@ def _load():
         lib.oracle_decode.argtypes = [P, I, I64, P]
         lib.oracle_round_bf16.argtypes = [P, I64, P]
         lib.oracle_wgrad_rows.argtypes = [P, P, I, I64, I64, I64, I64, D, D, P, I64, P]
+        lib.oracle_wgrad_rows_lowered.argtypes = [P, P, I, I64, I64, I64, I64, ctypes.c_float,
+                                                  ctypes.c_float, P, I64, I, P]
         lib.oracle_wgrad_elem.argtypes = [P, P, I, I64, I64, I64, I64, D, D, I64, I64]
         lib.oracle_wgrad_elem.restype = D
         lib.oracle_adamw.argtypes = [I64, P, P, P, P, I, D, D, D, D, D, I64, P, P, P, P, P, P]
@@ -173,6 +175,29 @@ def wgrad(X, dY, scales=(1.0, 1.0), rows=None, k_range=None) -> np.ndarray:
     G = np.empty((nr, M), np.float64)
     _load().oracle_wgrad_rows(_ptr(X), _ptr(dY), dt, M, N, kb, ke,
                               float(scales[0]), float(scales[1]), _ptr(r), nr, _ptr(G))
+    return G
+
+
+def wgrad_lowered(X, dY, scales=(1.0, 1.0), rows=None, truncate=True) -> np.ndarray:
+    """The unfused lowering: products added in ascending k into a float
+    accumulator, scaled by sX * sdY in float and, with ``truncate``, rounded
+    to bf16 (the "bf16 accumulate in f32 then truncf" the fused path deletes,
+    P6).  Returned widened to float64, [len(rows) or N, M]."""
+    X = as_bits(X)
+    dY = as_bits(dY)
+    dt = _dtype_of(X)
+    assert _dtype_of(dY) == dt and X.ndim == 2 and dY.ndim == 2 and X.shape[0] == dY.shape[0]
+    K, N = X.shape
+    M = dY.shape[1]
+    if rows is None:
+        r, nr = None, N
+    else:
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        nr = r.size
+    G = np.empty((nr, M), np.float64)
+    _load().oracle_wgrad_rows_lowered(_ptr(X), _ptr(dY), dt, M, N, 0, K, float(scales[0]),
+                                      float(scales[1]), _ptr(r), nr, 1 if truncate else 0,
+                                      _ptr(G))
     return G
 
 

@@ -45,6 +45,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* Element types; the numbers match the library's public enum by meaning, not
@@ -175,6 +176,39 @@ void oracle_wgrad_rows(const void* X, const void* dY, int in_dtype,
         }
         for (int64_t m = 0; m < M; ++m)
             g[m] = s * g[m];
+    }
+}
+
+/* The unfused lowering the fused path is measured against (P6, and "What's
+ * already in tree and easy to miss": the matmul lowering accumulates bf16
+ * products in f32 and then truncates to bf16).  Each product of two decoded
+ * inputs is exact in float (bf16 and e4m3 significands are short enough), and
+ * the products are added in ascending k into a float accumulator, one rounding
+ * per addition; the sum is scaled by sX * sdY in float and, with `truncate`,
+ * rounded to bf16 (nearest, ties to even).  Results are widened to double. */
+void oracle_wgrad_rows_lowered(const void* X, const void* dY, int in_dtype,
+                               int64_t M, int64_t N, int64_t k_begin, int64_t k_end,
+                               float sX, float sdY, const int64_t* rows, int64_t nrows,
+                               int truncate, double* G)
+{
+    const float s = sX * sdY;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nrows; ++i) {
+        const int64_t n = rows ? rows[i] : i;
+        float* acc = (float*)calloc((size_t)(M > 0 ? M : 1), sizeof(float));
+        double* g = G + i * M;
+        for (int64_t k = k_begin; k < k_end; ++k) {
+            const float x = (float)load_elem(X, in_dtype, k * N + n);
+            for (int64_t m = 0; m < M; ++m) {
+                const float p = x * (float)load_elem(dY, in_dtype, k * M + m);
+                acc[m] = acc[m] + p;
+            }
+        }
+        for (int64_t m = 0; m < M; ++m) {
+            const float r = acc[m] * s;
+            g[m] = truncate ? oracle_bf16_to_double(oracle_double_to_bf16((double)r)) : (double)r;
+        }
+        free(acc);
     }
 }
 

@@ -150,6 +150,45 @@ def test_wgrad_e4m3_matches_numpy():
     assert np.max(np.abs(G - ref)) <= 1e-12 * np.max(np.abs(ref))
 
 
+# ---- the unfused lowering (the P6 comparator) ---------------------------------
+
+def test_lowered_accumulates_in_float_in_ascending_k():
+    # 2^24 + 1 + 1: ascending k in float rounds 2^24 + 1 back to 2^24 (tie to
+    # even) twice; the reversed order keeps both ones; fp64 keeps them anyway
+    X = bf16_bits(torch.ones((3, 1)))
+    up = bf16_bits(torch.tensor([[2.0 ** 24], [1.0], [1.0]]))
+    down = bf16_bits(torch.tensor([[1.0], [1.0], [2.0 ** 24]]))
+    assert oracle.wgrad_lowered(X, up, truncate=False)[0, 0] == 2.0 ** 24
+    assert oracle.wgrad_lowered(X, down, truncate=False)[0, 0] == 2.0 ** 24 + 2
+    assert oracle.wgrad(X, up)[0, 0] == 2.0 ** 24 + 2
+
+
+def test_lowered_truncation_is_nearest_bf16_ties_to_even():
+    X = bf16_bits(torch.ones((3, 1)))
+    D = bf16_bits(torch.tensor([[1.0], [2.0 ** -8], [2.0 ** -9]]))
+    assert oracle.wgrad_lowered(X, D, truncate=False)[0, 0] == 1 + 2.0 ** -8 + 2.0 ** -9
+    assert oracle.wgrad_lowered(X, D, truncate=True)[0, 0] == 1 + 2.0 ** -7  # above the midpoint
+    tie = bf16_bits(torch.tensor([[1.0], [2.0 ** -8], [0.0]]))
+    assert oracle.wgrad_lowered(X, tie, truncate=True)[0, 0] == 1.0  # midpoint, even is below
+    tie_up = bf16_bits(torch.tensor([[1.0 + 2.0 ** -7], [2.0 ** -8], [0.0]]))
+    assert oracle.wgrad_lowered(X, tie_up, truncate=True)[0, 0] == 1 + 2.0 ** -6  # even is above
+
+
+def test_lowered_equals_exact_when_float_sums_are_exact():
+    rng = np.random.default_rng(3)
+    Xi = rng.integers(-8, 9, size=(40, 6)).astype(np.float32)
+    Di = rng.integers(-8, 9, size=(40, 5)).astype(np.float32)
+    X, D = bf16_bits(torch.from_numpy(Xi)), bf16_bits(torch.from_numpy(Di))
+    exact = Xi.astype(np.float64).T @ Di.astype(np.float64)  # integers below 2^24
+    assert np.array_equal(oracle.wgrad_lowered(X, D, truncate=False), exact)
+    trunc = torch.from_numpy(exact).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle.wgrad_lowered(X, D, truncate=True), trunc)
+    assert np.array_equal(oracle.wgrad_lowered(X, D, scales=(0.5, 0.25), truncate=False),
+                          exact * 0.125)
+    assert np.array_equal(oracle.wgrad_lowered(X, D, rows=[4, 1], truncate=False),
+                          exact[[4, 1]])
+
+
 # ---- AdamW -------------------------------------------------------------------
 
 HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.01)
