@@ -63,6 +63,9 @@ def _load():
         lib.oracle_bf16_to_double.restype = D
         lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_to_double.restype = D
+        lib.oracle_double_to_e4m3.argtypes = [D]
+        lib.oracle_double_to_e4m3.restype = ctypes.c_uint8
+        lib.oracle_quantize_e4m3.argtypes = [P, I, I64, P, P]
         lib.oracle_double_to_bf16.argtypes = [D]
         lib.oracle_double_to_bf16.restype = ctypes.c_uint16
         lib.oracle_decode.argtypes = [P, I, I64, P]
@@ -149,6 +152,26 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
     out = np.empty(x.shape, np.uint16)
     _load().oracle_round_bf16(_ptr(x), x.size, _ptr(out))
     return out
+
+
+# ---- fp8 quantisation ------------------------------------------------------
+
+def double_to_e4m3(x: float) -> int:
+    """Nearest e4m3fn code, ties to even, saturating at 448; NaN -> 0x7F."""
+    return int(_load().oracle_double_to_e4m3(float(x)))
+
+
+def quantize_e4m3(x):
+    """Per-tensor e4m3 quantisation: (codes uint8 array, scale float) with
+    scale = amax / 448 in float (1 when amax is 0) and codes = nearest e4m3 of
+    the float quotient x / scale.  x: fp32 array or raw bf16 patterns."""
+    x = as_bits(x)
+    dt = _dtype_of(x)
+    assert dt in (BF16, F32)
+    codes = np.empty(x.shape, np.uint8)
+    sc = ctypes.c_float(0.0)
+    _load().oracle_quantize_e4m3(_ptr(x), dt, x.size, _ptr(codes), ctypes.byref(sc))
+    return codes, float(sc.value)
 
 
 # ---- the contraction ------------------------------------------------------

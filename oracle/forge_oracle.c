@@ -130,6 +130,64 @@ static double load_elem(const void* base, int dtype, int64_t i)
     return (double)((const float*)base)[i];
 }
 
+/* ---- fp8 quantisation ------------------------------------------------------ */
+
+/* The e4m3fn code of the finite value nearest to x, ties to the code with an
+ * even mantissa; magnitudes from 448 up saturate to 448 and NaN gives 0x7F.
+ * Codes 0..126 are the non-negative finite values in increasing order (code
+ * 127 is NaN), so the two neighbours of |x| are found by bisection over the
+ * decoded values. */
+uint8_t oracle_double_to_e4m3(double x)
+{
+    uint8_t sign;
+    double a, vlo, vhi;
+    int lo = 0, hi = 126;
+    if (isnan(x))
+        return 0x7F;
+    sign = signbit(x) ? 0x80 : 0x00;
+    a = fabs(x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    while (lo < hi) { /* largest code whose value is <= a */
+        int mid = (lo + hi + 1) / 2;
+        if (oracle_e4m3_to_double((uint8_t)mid) <= a)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    vlo = oracle_e4m3_to_double((uint8_t)lo);
+    if (vlo == a)
+        return (uint8_t)(sign | lo);
+    vhi = oracle_e4m3_to_double((uint8_t)(lo + 1));
+    if (a - vlo < vhi - a)
+        return (uint8_t)(sign | lo);
+    if (vhi - a < a - vlo)
+        return (uint8_t)(sign | (lo + 1));
+    return (uint8_t)(sign | ((lo & 1) ? lo + 1 : lo)); /* a tie: the even code */
+}
+
+/* Per-tensor e4m3 quantisation with an amax scale (the fp8 recipe, s =
+ * amax / 448): amax = max |x| over the n inputs (fp32 values or bf16
+ * patterns; NaN entries are skipped), s = amax / 448 divided in float (1 when
+ * amax is 0), and each code is the e4m3 value nearest to the float quotient
+ * x / s. */
+void oracle_quantize_e4m3(const void* x, int dtype, int64_t n, uint8_t* codes, float* scale)
+{
+    double amax = 0.0;
+    float s;
+    for (int64_t i = 0; i < n; ++i) {
+        const double a = fabs(load_elem(x, dtype, i));
+        if (a > amax)
+            amax = a;
+    }
+    s = amax > 0.0 ? (float)amax / 448.0f : 1.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        const float t = (float)load_elem(x, dtype, i) / s;
+        codes[i] = oracle_double_to_e4m3((double)t);
+    }
+    *scale = s;
+}
+
 void oracle_decode(const void* src, int dtype, int64_t n, double* dst)
 {
     for (int64_t i = 0; i < n; ++i)

@@ -150,6 +150,71 @@ def test_wgrad_e4m3_matches_numpy():
     assert np.max(np.abs(G - ref)) <= 1e-12 * np.max(np.abs(ref))
 
 
+# ---- fp8 quantisation ------------------------------------------------------------
+
+def e4m3_values():
+    codes = np.arange(256, dtype=np.uint8)
+    return codes, oracle.decode(codes)
+
+
+def test_e4m3_encode_round_trips_every_finite_code():
+    codes, vals = e4m3_values()
+    for c, v in zip(codes, vals):
+        if np.isnan(v):
+            continue
+        assert oracle.double_to_e4m3(v) == c, (c, v)
+    assert oracle.double_to_e4m3(float("nan")) == 0x7F
+
+
+def test_e4m3_encode_midpoints_go_to_the_even_code_and_saturate():
+    codes, vals = e4m3_values()
+    for c in range(126):  # consecutive non-negative finite codes c, c + 1
+        mid = (Fraction(float(vals[c])) + Fraction(float(vals[c + 1]))) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.double_to_e4m3(float(mid)) == even, c
+        assert oracle.double_to_e4m3(-float(mid)) == 0x80 | even, c
+        # just off the midpoint: the nearer neighbour
+        below = float(vals[c]) + 0.49 * (float(vals[c + 1]) - float(vals[c]))
+        assert oracle.double_to_e4m3(below) == c
+    assert oracle.double_to_e4m3(448.0) == 0x7E
+    assert oracle.double_to_e4m3(1e9) == 0x7E
+    assert oracle.double_to_e4m3(-500.0) == 0xFE
+    assert oracle.double_to_e4m3(-0.0) == 0x80
+
+
+def test_e4m3_encode_matches_torch_cast_in_range():
+    t = torch.cat([wl.randn((20000,), 31, std=50.0),
+                   wl.randn((20000,), 32, std=2.0 ** -8)]).clamp(-448.0, 448.0)
+    want = t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.double_to_e4m3(float(v)) for v in t.numpy()], dtype=np.uint8)
+    assert np.array_equal(got, want)
+
+
+def test_quantize_matches_the_amax_recipe():
+    t = wl.with_outliers((3000,), 33)
+    codes, s = oracle.quantize_e4m3(t.numpy())
+    want, ws = wl.quantize_e4m3(t)
+    assert s == ws == float(np.float32(float(t.abs().max()) / 448.0))
+    assert np.array_equal(codes, want.view(torch.uint8).numpy())
+    # bf16 input: the same recipe on the widened values
+    b = wl.randn((999,), 34, std=3.0).to(torch.bfloat16)
+    codes, s = oracle.quantize_e4m3(b)
+    want, ws = wl.quantize_e4m3(b.to(torch.float32))
+    assert s == ws and np.array_equal(codes, want.view(torch.uint8).numpy())
+    # the largest magnitude maps to 448 exactly
+    at_amax = np.abs(b.float().numpy()) == float(b.abs().max())
+    assert np.all(np.abs(oracle.decode(codes[at_amax])) == 448.0)
+
+
+def test_quantize_degenerate_inputs():
+    codes, s = oracle.quantize_e4m3(np.zeros(17, np.float32))
+    assert s == 1.0 and not codes.any()
+    codes, s = oracle.quantize_e4m3(np.zeros(0, np.float32))
+    assert s == 1.0 and codes.size == 0
+    codes, s = oracle.quantize_e4m3(np.array([-2.0, 1.0], np.float32))
+    assert s == np.float32(2.0 / 448.0) and oracle.decode(codes)[0] == -448.0
+
+
 # ---- the unfused lowering (the P6 comparator) ---------------------------------
 
 def test_lowered_accumulates_in_float_in_ascending_k():
