@@ -156,6 +156,9 @@ class Dense:
         es = 4 if state_dtype == torch.float32 else 2
         # algorithmic bytes: X and dY read once, W read+write, m and v read+write
         self.bytes = (K * N + K * M) * 2 + N * M * (8 + 4 * es)
+        # the fused kernel, plus a staging copy per operand whose rows are not
+        # a multiple of 16 bytes
+        self.launches = 1 + int((2 * N) % 16 != 0) + int((2 * M) % 16 != 0)
 
     peak_key = "bf16"
     opt = "AdamW"
@@ -181,7 +184,7 @@ class Dense:
 class AttnSet:
     """The four attention projections of one layer (d_in 4096, d_out 4096,
     1024, 1024, 4100; K = 16384) as four fused calls per step; d_out = 4100
-    has 8200-byte dY rows and goes through the cp.async loader."""
+    has 8200-byte dY rows, which the library stages into 16-byte rows."""
 
     peak_key = "bf16"
     opt = "AdamW"
@@ -196,6 +199,7 @@ class AttnSet:
         self.flops = sum(p.flops for p in self.parts)
         self.params = sum(p.params for p in self.parts)
         self.bytes = sum(p.bytes for p in self.parts)
+        self.launches = sum(p.launches for p in self.parts)
 
     def step(self, stream=None):
         for p in self.parts:
@@ -243,6 +247,7 @@ class MoE:
         self.params = E * N * M
         es = 4 if state_dtype == torch.float32 else 2
         self.bytes = 2 * (T * N + T * M) + E * N * M * (8 + 4 * es)
+        self.launches = 1
 
     def step(self, stream=None, X=None, D=None):
         import weight_grad_gemm_gb300 as fg
@@ -288,6 +293,7 @@ class Fp8:
         es = 4 if state_dtype == torch.float32 else 2
         nst = 2 if opt == "AdamW" else 1
         self.bytes = (K * N + K * M) + N * M * (8 + 2 * nst * es)
+        self.launches = 1
 
     def step(self, stream=None, X=None, D=None):
         import weight_grad_gemm_gb300 as fg
@@ -311,6 +317,55 @@ class Fp8:
 
     def result(self):
         return self.W
+
+
+class Fp8Quant(Fp8):
+    """The fp8 path from fp32 activations: every step quantises X and dY
+    [32768, 8192] with the library (amax pass + e4m3 codes, two launches
+    each), then runs the fused e4m3 AdamW call on the codes and scales."""
+
+    def __init__(self, dev, state_dtype=torch.float32):
+        super().__init__(dev, state_dtype, "AdamW")
+        wk = self.wk
+        K, N, M = wk.K, wk.N, wk.M
+        self.xf = wl.with_outliers((K, N), wl.seed_of(wk.name, "X"), dev)
+        self.yf = wl.with_outliers((K, M), wl.seed_of(wk.name, "dY"), dev)
+        self.X = torch.empty((K, N), dtype=torch.float8_e4m3fn, device=dev)
+        self.D = torch.empty((K, M), dtype=torch.float8_e4m3fn, device=dev)
+        # two passes over each fp32 input (amax, then codes) and the codes written
+        self.quant_bytes = 9 * (K * N + K * M)
+        self.bytes += self.quant_bytes
+        self.launches = 5
+        self.wk = wl.Workload(f"fp8_quant K={K} d_in={N} d_out={M} (fp32 X, dY quantised to "
+                              "e4m3 each step)", K=K, N=N, M=M)
+
+    def quantize(self, xf, yf, stream=None):
+        import weight_grad_gemm_gb300 as fg
+        fg.forge_quantize_e4m3(xf, self.X, self.scales[0:1], stream=stream)
+        fg.forge_quantize_e4m3(yf, self.D, self.scales[1:2], stream=stream)
+
+    def step(self, stream=None, X=None, D=None):
+        self.quantize(self.xf if X is None else X, self.yf if D is None else D, stream)
+        super().step(stream=stream)
+
+    def inputs(self):
+        return [self.xf, self.yf]
+
+    def parts_us(self, stream, flush, reps=5):
+        """Median device time of the quantisation and of the fused call."""
+        q, f = [], []
+        for _ in range(reps):
+            flush.zero_()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev[0].record(stream)
+            self.quantize(self.xf, self.yf, stream)
+            ev[1].record(stream)
+            Fp8.step(self, stream=stream)
+            ev[2].record(stream)
+            ev[2].synchronize()
+            q.append(ev[0].elapsed_time(ev[1]) * 1e3)
+            f.append(ev[1].elapsed_time(ev[2]) * 1e3)
+        return float(np.median(q)), float(np.median(f))
 
 
 class Unfused:
@@ -357,6 +412,7 @@ WORKLOADS = {
     "moe": lambda dev, st: MoE(dev, st),
     "fp8": lambda dev, st: Fp8(dev, st, "AdamW"),
     "fp8_sgdm": lambda dev, st: Fp8(dev, st, "SGD"),
+    "fp8_quant": lambda dev, st: Fp8Quant(dev, st),
 }
 
 
@@ -599,10 +655,16 @@ def main():
                      "peak_source": peak_note, "traffic": traffic},
         "e2e": {"value": job.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * len(getattr(job, "parts", [None])) if args.impl == "ours" else 0,
+        "gpu_launches": args.steps * getattr(job, "launches", 1) if args.impl == "ours" else 0,
         "clocks": clk,
         "wall_s_timed_region": wall,
     }
+    if isinstance(job, Fp8Quant):
+        q_us, f_us = job.parts_us(stream, flush)
+        gbs = job.quant_bytes / (q_us * 1e-6) / 1e9
+        line["quantize"] = {"us": q_us, "fused_us": f_us, "bound": "hbm", "achieved": gbs,
+                            "peak": bw, "unit": "GB/s", "frac": gbs / bw,
+                            "bytes": job.quant_bytes}
     if (rank == 0 and world == 1 and not args.no_cpu_baseline and args.impl == "ours" and
             isinstance(job, Dense)):
         line["cpu_baseline"] = cpu_baseline(job)

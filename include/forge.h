@@ -37,7 +37,8 @@
  *
  * Ownership and ordering: every pointer is caller-owned device memory and
  * the library keeps no pointer after the call returns.  It allocates nothing
- * per call, with one exception: an operand (X or dY) whose base is not
+ * per call, with two exceptions: forge_quantize_e4m3 takes a few bytes of
+ * scratch per call (see there), and an operand (X or dY) whose base is not
  * 16-byte aligned or whose row stride is not a multiple of 16 bytes is first
  * copied into a padded scratch buffer taken from the device's default memory
  * pool with cudaMallocAsync on `stream` and returned with cudaFreeAsync on
@@ -155,6 +156,29 @@ FORGE_API forge_status forge_wgrad_adamw_noalloc(const void* X, const void* dY, 
                                                  float lr, float beta1, float beta2, float eps,
                                                  float wd, int64_t step, const float* scales,
                                                  forge_stream_t stream);
+
+/*
+ * Per-tensor e4m3 quantisation with an amax scale, the step in front of an
+ * fp8 call (the fp8 rows of "Math verified, not asserted", P6; the recipe
+ * s = amax / 448 of the fp8 workload):
+ *   x       device [n] of x_dtype (FORGE_F32 or FORGE_BF16), read as a flat
+ *           array (any tensor shape, row-major).
+ *   codes   device [n] bytes: OCP e4m3fn codes, each the value nearest to
+ *           x / s computed in fp32 (ties to even; magnitudes past 448 saturate).
+ *   scale   device float[1]: receives s = amax|x| / 448 (an fp32 division),
+ *           or 1 when amax is 0 (n == 0 included).  NaN entries of x are left
+ *           out of the amax (their codes are NaN).
+ * Pass codes and scale as X (or dY) and scales[0] (or scales[1]) of an e4m3
+ * call.  Two passes over x: the first writes one partial maximum per block
+ * (at most four blocks per SM) into a scratch array taken from the device's
+ * default memory pool with cudaMallocAsync on `stream`, returned with
+ * cudaFreeAsync after the second.  Errors: n < 0, scale NULL, or x / codes
+ * NULL with n > 0 -> FORGE_ERR_INVALID_ARG; x_dtype -> FORGE_ERR_UNSUPPORTED_DTYPE;
+ * x not aligned to its element size or scale not 4-byte aligned ->
+ * FORGE_ERR_MISALIGNED.
+ */
+FORGE_API forge_status forge_quantize_e4m3(const void* x, forge_dtype x_dtype, int64_t n,
+                                           uint8_t* codes, float* scale, forge_stream_t stream);
 
 /*
  * Fused dW = X^T dY and one SGD-momentum step on W and the momentum buffer

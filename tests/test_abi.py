@@ -113,6 +113,18 @@ def test_grouped_rejects_invalid_arguments(L):
     assert g(step=0) == fg.FORGE_ERR_INVALID_ARG
 
 
+def test_quantize_rejects_invalid_arguments(L):
+    def q(x=FAKE, dt=fg.FORGE_F32, n=64, codes=FAKE, scale=FAKE):
+        return L.forge_quantize_e4m3(x, dt, n, codes, scale, None)
+    assert q(n=-1) == fg.FORGE_ERR_INVALID_ARG
+    assert q(scale=None) == fg.FORGE_ERR_INVALID_ARG
+    assert q(x=None) == fg.FORGE_ERR_INVALID_ARG
+    assert q(codes=None) == fg.FORGE_ERR_INVALID_ARG
+    assert q(dt=fg.FORGE_E4M3) == fg.FORGE_ERR_UNSUPPORTED_DTYPE
+    assert q(x=ctypes.c_void_p(0x10002)) == fg.FORGE_ERR_MISALIGNED
+    assert q(scale=ctypes.c_void_p(0x10001)) == fg.FORGE_ERR_MISALIGNED
+
+
 def test_selftest_rejects_bad_limit(L):
     assert L.forge_selftest_wait_timeout(0, None) == fg.FORGE_ERR_INVALID_ARG
 

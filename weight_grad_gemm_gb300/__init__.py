@@ -34,6 +34,7 @@ FORGE_E4M3 = 1
 FORGE_F32 = 2
 
 EXPORTS = ("forge_wgrad_adamw", "forge_wgrad_adamw_noalloc", "forge_wgrad_sgdm", "forge_wgrad_only",
+           "forge_quantize_e4m3",
            "forge_grouped_wgrad_adamw", "forge_status_string", "forge_get_device_status",
            "forge_selftest_wait_timeout", "forge_version")
 
@@ -59,12 +60,13 @@ def lib() -> ctypes.CDLL:
                          ctypes.c_int)
     L.forge_wgrad_adamw.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, F, F, F, F, F, I64, P, P]
     L.forge_wgrad_adamw_noalloc.argtypes = L.forge_wgrad_adamw.argtypes
+    L.forge_quantize_e4m3.argtypes = [P, I, I64, P, P, P]
     L.forge_wgrad_sgdm.argtypes = [P, P, P, P, I64, I64, I64, I, I, F, F, F, P, P]
     L.forge_wgrad_only.argtypes = [P, P, P, I64, I64, I64, I, P, P]
     L.forge_grouped_wgrad_adamw.argtypes = [P, P, P, P, P, P, I32, I64, I64, I64, I, I, F, F, F,
                                             F, F, I64, P, P]
     for f in ("forge_wgrad_adamw", "forge_wgrad_adamw_noalloc", "forge_wgrad_sgdm",
-              "forge_wgrad_only",
+              "forge_wgrad_only", "forge_quantize_e4m3",
               "forge_grouped_wgrad_adamw", "forge_get_device_status",
               "forge_selftest_wait_timeout"):
         getattr(L, f).restype = I
@@ -175,6 +177,20 @@ def forge_wgrad_only(X, dY, dW, *, scales=None, stream=None):
     s = lib().forge_wgrad_only(_ptr(X), _ptr(dY), _ptr(dW), M, N, K, _dtype_code(X),
                                _scales_ptr(scales, X), _stream(stream, dW))
     _check(s, "forge_wgrad_only")
+
+
+def forge_quantize_e4m3(x, codes, scale, *, stream=None):
+    """codes (uint8 or float8_e4m3fn, x.numel() elements) and scale (float32
+    [1]) from x (float32 or bfloat16): s = amax / 448, codes = nearest e4m3 of
+    x / s."""
+    import torch
+    if codes.numel() != x.numel() or codes.element_size() != 1:
+        raise ValueError("codes must hold one byte per element of x")
+    if scale.dtype != torch.float32 or scale.numel() != 1:
+        raise ValueError("scale must be a float32 tensor of one element")
+    s = lib().forge_quantize_e4m3(_ptr(x), _dtype_code(x), x.numel(), _ptr(codes), _ptr(scale),
+                                  _stream(stream, codes))
+    _check(s, "forge_quantize_e4m3")
 
 
 def forge_grouped_wgrad_adamw(X, dY, W, m, v, offsets, *, lr, beta1, beta2, eps, wd, step,

@@ -23,8 +23,9 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libforge.so")
 
 SOURCES = ["forge_api.cu", "kernels_bf16.cu", "kernels_e4m3.cu", "kernels_pair_bf16.cu",
-           "kernels_pair_e4m3.cu", "forge_static_stage.cu"]
-HEADERS = ["forge_ptx.cuh", "forge_kernel.cuh", "forge_launch.cuh", "forge_static_stage.h"]
+           "kernels_pair_e4m3.cu", "forge_static_stage.cu", "forge_quant.cu"]
+HEADERS = ["forge_ptx.cuh", "forge_kernel.cuh", "forge_launch.cuh", "forge_static_stage.h",
+           "forge_device.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

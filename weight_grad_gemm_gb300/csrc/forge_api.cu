@@ -19,6 +19,7 @@
 #include <mutex>
 
 #include "forge.h"
+#include "forge_device.h"
 #include "forge_launch.cuh"
 #include "forge_static_stage.h"
 
@@ -489,6 +490,14 @@ void fill_adam(Params& p, float lr, float beta1, float beta2, float eps, float w
 }
 
 }  // namespace
+
+forge_status forge::device_sms(int* sms)
+{
+    DeviceInfo* dev = nullptr;
+    const forge_status st = current_device(&dev);
+    if (st == FORGE_OK) *sms = dev->sms;
+    return st;
+}
 
 extern "C" {
 
