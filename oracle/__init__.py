@@ -74,6 +74,7 @@ def _load():
         lib.oracle_wgrad_rows_lowered.argtypes = [P, P, I, I64, I64, I64, I64, ctypes.c_float,
                                                   ctypes.c_float, P, I64, I, P]
         lib.oracle_wgrad_elem.argtypes = [P, P, I, I64, I64, I64, I64, D, D, I64, I64]
+        lib.oracle_dgrad_rows.argtypes = [P, P, I64, I64, P, I64, P]
         lib.oracle_wgrad_elem.restype = D
         lib.oracle_adamw.argtypes = [I64, P, P, P, P, I, D, D, D, D, D, I64, P, P, P, P, P, P]
         lib.oracle_sgdm.argtypes = [I64, P, P, P, I, D, D, D, P, P, P, P]
@@ -221,6 +222,25 @@ def wgrad_lowered(X, dY, scales=(1.0, 1.0), rows=None, truncate=True) -> np.ndar
     _load().oracle_wgrad_rows_lowered(_ptr(X), _ptr(dY), dt, M, N, 0, K, float(scales[0]),
                                       float(scales[1]), _ptr(r), nr, 1 if truncate else 0,
                                       _ptr(G))
+    return G
+
+
+def dgrad(dY, Wb, rows=None) -> np.ndarray:
+    """dX = dY Wb^T in float64, [len(rows) or K, N]: dY [K, M] and Wb [N, M]
+    raw bf16 arrays; rows selects token rows of dX."""
+    dY = as_bits(dY)
+    Wb = as_bits(Wb)
+    assert _dtype_of(dY) == BF16 and _dtype_of(Wb) == BF16
+    K, M = dY.shape
+    N, M2 = Wb.shape
+    assert M == M2
+    if rows is None:
+        r, nr = None, K
+    else:
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        nr = r.size
+    G = np.empty((nr, N), np.float64)
+    _load().oracle_dgrad_rows(_ptr(dY), _ptr(Wb), M, N, _ptr(r), nr, _ptr(G))
     return G
 
 

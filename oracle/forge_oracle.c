@@ -181,6 +181,7 @@ void oracle_quantize_e4m3(const void* x, int dtype, int64_t n, uint8_t* codes, f
             amax = a;
     }
     s = amax > 0.0 ? (float)amax / 448.0f : 1.0f;
+#pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) {
         const float t = (float)load_elem(x, dtype, i) / s;
         codes[i] = oracle_double_to_e4m3((double)t);
@@ -267,6 +268,26 @@ void oracle_wgrad_rows_lowered(const void* X, const void* dY, int in_dtype,
             g[m] = truncate ? oracle_bf16_to_double(oracle_double_to_bf16((double)r)) : (double)r;
         }
         free(acc);
+    }
+}
+
+/* The input gradient on the other side of the backward pass (the dX that
+ * must read W before the in-place update, "Math verified, not asserted", P1):
+ * dX[k][n] = sum over m of dY[k][m] * Wb[n][m], with dY [K, M] and the weight
+ * Wb [N, M] both bf16 patterns, summed in ascending m in double, for the
+ * token rows `rows` (or all K rows when rows is NULL).  G is [nrows, N]. */
+void oracle_dgrad_rows(const uint16_t* dY, const uint16_t* Wb, int64_t M, int64_t N,
+                       const int64_t* rows, int64_t nrows, double* G)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nrows; ++i) {
+        const int64_t k = rows ? rows[i] : i;
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m)
+                acc += oracle_bf16_to_double(dY[k * M + m]) * oracle_bf16_to_double(Wb[n * M + m]);
+            G[i * N + n] = acc;
+        }
     }
 }
 

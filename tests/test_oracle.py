@@ -150,6 +150,33 @@ def test_wgrad_e4m3_matches_numpy():
     assert np.max(np.abs(G - ref)) <= 1e-12 * np.max(np.abs(ref))
 
 
+# ---- the input gradient dX = dY W^T -------------------------------------------
+
+def test_dgrad_bruteforce_integers():
+    rng = np.random.default_rng(41)
+    Di = rng.integers(-5, 6, size=(6, 9))
+    Wi = rng.integers(-5, 6, size=(4, 9))
+    D = bf16_bits(torch.tensor(Di, dtype=torch.float32))
+    Wb = bf16_bits(torch.tensor(Wi, dtype=torch.float32))
+    want = np.array([[sum(int(Di[k, m]) * int(Wi[n, m]) for m in range(9)) for n in range(4)]
+                     for k in range(6)], dtype=np.float64)
+    assert np.array_equal(oracle.dgrad(D, Wb), want)
+    assert np.array_equal(oracle.dgrad(D, Wb, rows=[5, 0]), want[[5, 0]])
+
+
+def test_dgrad_orientation_and_numpy():
+    # Wb = I (N = M) gives dX = dY; Wb = one row of ones sums dY's rows
+    D = rand_bf16((7, 12), 42)
+    eye = bf16_bits(torch.eye(12))
+    assert np.array_equal(oracle.dgrad(D, eye), oracle.decode(D))
+    ones = bf16_bits(torch.ones((1, 12)))
+    assert np.allclose(oracle.dgrad(D, ones)[:, 0], oracle.decode(D).sum(axis=1), rtol=0,
+                       atol=1e-12)
+    Wb = rand_bf16((20, 12), 43)
+    ref = oracle.decode(D) @ oracle.decode(Wb).T
+    assert np.max(np.abs(oracle.dgrad(D, Wb) - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
 # ---- fp8 quantisation ------------------------------------------------------------
 
 def e4m3_values():
