@@ -181,6 +181,52 @@ class Dense:
         return self.W
 
 
+class Backward(Dense):
+    """The MLP down-projection's whole backward-and-update step through
+    forge_backward_adamw: dX = dY Wb^T from the forward's bf16 weight copy,
+    then the fused dW + AdamW, ordered on one stream."""
+
+    def __init__(self, dev, state_dtype=torch.float32):
+        super().__init__(wl.MLP_DOWN, dev, state_dtype)
+        wk = self.wk
+        K, N, M = wk.K, wk.N, wk.M
+        self.Wb = self.W.to(torch.bfloat16)
+        self.dX = torch.empty((K, N), dtype=torch.bfloat16, device=dev)
+        self.flops = 2 * wk.flops
+        # the input gradient reads dY and Wb and writes dX
+        self.bytes += 2 * (K * M + N * M + K * N)
+        self.launches = 2
+        self.wk = wl.Workload(f"backward K={K} d_in={N} d_out={M} (dX = dY W^T, then fused "
+                              "dW + AdamW)", K=K, N=N, M=M)
+
+    def step(self, X=None, D=None, stream=None):
+        import weight_grad_gemm_gb300 as fg
+        if not hasattr(self, "Wb"):  # the warm-up steps of the constructor
+            return Dense.step(self, X, D, stream)
+        hp = self.hp
+        fg.forge_backward_adamw(self.X if X is None else X, self.D if D is None else D, self.W,
+                                self.m, self.v, self.dX, Wb=self.Wb, lr=hp.lr, beta1=hp.beta1,
+                                beta2=hp.beta2, eps=hp.eps, wd=hp.wd, step=self.t, stream=stream)
+        self.t += 1
+
+    def parts_us(self, stream, flush, reps=5):
+        """Median device time of the input gradient and of the fused call."""
+        import weight_grad_gemm_gb300 as fg
+        a, b = [], []
+        for _ in range(reps):
+            flush.zero_()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev[0].record(stream)
+            fg.forge_dgrad(self.D, self.Wb, self.dX, stream=stream)
+            ev[1].record(stream)
+            Dense.step(self, stream=stream)
+            ev[2].record(stream)
+            ev[2].synchronize()
+            a.append(ev[0].elapsed_time(ev[1]) * 1e3)
+            b.append(ev[1].elapsed_time(ev[2]) * 1e3)
+        return float(np.median(a)), float(np.median(b))
+
+
 class AttnSet:
     """The four attention projections of one layer (d_in 4096, d_out 4096,
     1024, 1024, 4100; K = 16384) as four fused calls per step; d_out = 4100
@@ -413,6 +459,7 @@ WORKLOADS = {
     "fp8": lambda dev, st: Fp8(dev, st, "AdamW"),
     "fp8_sgdm": lambda dev, st: Fp8(dev, st, "SGD"),
     "fp8_quant": lambda dev, st: Fp8Quant(dev, st),
+    "backward": lambda dev, st: Backward(dev, st),
 }
 
 
@@ -659,6 +706,12 @@ def main():
         "clocks": clk,
         "wall_s_timed_region": wall,
     }
+    if isinstance(job, Backward):
+        d_us, f_us = job.parts_us(stream, flush)
+        wk = job.wk
+        tf = 2.0 * wk.K * wk.N * wk.M / (d_us * 1e-6) / 1e12
+        line["dgrad"] = {"us": d_us, "fused_us": f_us, "bound": "tensor", "achieved": tf,
+                         "peak": peak_tf, "unit": "TFLOP/s", "frac": tf / peak_tf}
     if isinstance(job, Fp8Quant):
         q_us, f_us = job.parts_us(stream, flush)
         gbs = job.quant_bytes / (q_us * 1e-6) / 1e9
@@ -666,7 +719,7 @@ def main():
                             "peak": bw, "unit": "GB/s", "frac": gbs / bw,
                             "bytes": job.quant_bytes}
     if (rank == 0 and world == 1 and not args.no_cpu_baseline and args.impl == "ours" and
-            isinstance(job, Dense)):
+            type(job) is Dense):
         line["cpu_baseline"] = cpu_baseline(job)
     if rank == 0:
         print(json.dumps(line), flush=True)

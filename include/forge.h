@@ -37,8 +37,9 @@
  *
  * Ownership and ordering: every pointer is caller-owned device memory and
  * the library keeps no pointer after the call returns.  It allocates nothing
- * per call, with two exceptions: forge_quantize_e4m3 takes a few bytes of
- * scratch per call (see there), and an operand (X or dY) whose base is not
+ * per call, with three exceptions: forge_quantize_e4m3 takes a few bytes of
+ * scratch per call and forge_backward_adamw without a bf16 weight copy takes
+ * one (see there), and an operand (X or dY) whose base is not
  * 16-byte aligned or whose row stride is not a multiple of 16 bytes is first
  * copied into a padded scratch buffer taken from the device's default memory
  * pool with cudaMallocAsync on `stream` and returned with cudaFreeAsync on
@@ -179,6 +180,40 @@ FORGE_API forge_status forge_wgrad_adamw_noalloc(const void* X, const void* dY, 
  */
 FORGE_API forge_status forge_quantize_e4m3(const void* x, forge_dtype x_dtype, int64_t n,
                                            uint8_t* codes, float* scale, forge_stream_t stream);
+
+/*
+ * The input gradient dX = dY W^T (bf16 in, fp32 accumulation, bf16 out,
+ * nearest even), the GEMM on the other side of the backward pass that must
+ * read W before the fused update overwrites it ("Math verified, not
+ * asserted", P1).
+ *   dY  device [K, M] bf16 (the same tensor the weight gradient reads).
+ *   Wb  device [N, M] bf16: the weight as the forward pass used it (for a
+ *       fp32 master W, its bf16 copy).
+ *   dX  device [K, N] bf16, written.
+ * in_dtype must be FORGE_BF16.  dY and Wb need 16-byte aligned bases and a
+ * row stride (M * 2 bytes) that is a multiple of 16 (else
+ * FORGE_ERR_MISALIGNED); K may be 0 (nothing is written).
+ */
+FORGE_API forge_status forge_dgrad(const void* dY, const void* Wb, void* dX, int64_t M, int64_t N,
+                                   int64_t K, forge_dtype in_dtype, forge_stream_t stream);
+
+/*
+ * One backward-and-update step for a linear layer, in the order the in-place
+ * update requires: dX = dY Wb^T first, then the fused dW = X^T dY + AdamW on
+ * W, m, v (exactly forge_wgrad_adamw), both on `stream`, so dX always sees
+ * the weights from before this step.  Wb is the bf16 copy of W the forward
+ * pass used; with Wb == NULL the library first rounds W to bf16 (nearest
+ * even) into a stream-ordered scratch copy (N * M * 2 bytes, cudaMallocAsync
+ * / cudaFreeAsync on `stream`).  bf16 inputs only.  Every argument check of
+ * both halves runs before the first launch; the arguments are those of
+ * forge_dgrad and forge_wgrad_adamw.
+ */
+FORGE_API forge_status forge_backward_adamw(const void* X, const void* dY, float* W, void* m,
+                                            void* v, const void* Wb, void* dX, int64_t M,
+                                            int64_t N, int64_t K, forge_dtype in_dtype,
+                                            forge_dtype state_dtype, float lr, float beta1,
+                                            float beta2, float eps, float wd, int64_t step,
+                                            forge_stream_t stream);
 
 /*
  * Fused dW = X^T dY and one SGD-momentum step on W and the momentum buffer

@@ -125,6 +125,28 @@ def test_quantize_rejects_invalid_arguments(L):
     assert q(scale=ctypes.c_void_p(0x10001)) == fg.FORGE_ERR_MISALIGNED
 
 
+def test_dgrad_and_backward_reject_invalid_arguments(L):
+    def d(dY=FAKE, Wb=FAKE, dX=FAKE, M=64, N=64, K=64, dt=fg.FORGE_BF16):
+        return L.forge_dgrad(dY, Wb, dX, M, N, K, dt, None)
+    assert d(Wb=None) == fg.FORGE_ERR_INVALID_ARG
+    assert d(dX=None) == fg.FORGE_ERR_INVALID_ARG
+    assert d(M=0) == fg.FORGE_ERR_INVALID_ARG
+    assert d(K=-1) == fg.FORGE_ERR_INVALID_ARG
+    assert d(dt=fg.FORGE_E4M3) == fg.FORGE_ERR_UNSUPPORTED_DTYPE
+    assert d(M=60) == fg.FORGE_ERR_MISALIGNED          # 120-byte rows
+    assert d(Wb=ctypes.c_void_p(0x10008)) == fg.FORGE_ERR_MISALIGNED
+
+    def b(W=FAKE, Wb=FAKE, hp=HP, step=1, dt=fg.FORGE_BF16, st=fg.FORGE_F32):
+        return L.forge_backward_adamw(FAKE, FAKE, W, FAKE, FAKE, Wb, FAKE, 64, 64, 64, dt, st,
+                                      *hp, step, None)
+    assert b(W=None) == fg.FORGE_ERR_INVALID_ARG
+    assert b(step=0) == fg.FORGE_ERR_INVALID_ARG
+    assert b(hp=(1e-3, 1.5, 0.999, 1e-8, 0.0)) == fg.FORGE_ERR_INVALID_ARG
+    assert b(dt=fg.FORGE_E4M3) == fg.FORGE_ERR_UNSUPPORTED_DTYPE
+    assert b(st=fg.FORGE_E4M3) == fg.FORGE_ERR_UNSUPPORTED_DTYPE
+    assert b(W=ctypes.c_void_p(0x10002)) == fg.FORGE_ERR_MISALIGNED
+
+
 def test_selftest_rejects_bad_limit(L):
     assert L.forge_selftest_wait_timeout(0, None) == fg.FORGE_ERR_INVALID_ARG
 
@@ -135,4 +157,6 @@ def test_valid_call_without_gpu_fails_closed(L):
         pytest.skip("a GPU is present; the fake pointers must not reach a kernel")
     assert adamw(L) == fg.FORGE_ERR_UNSUPPORTED_DEVICE
     assert adamw(L, fn="forge_wgrad_adamw_noalloc") == fg.FORGE_ERR_UNSUPPORTED_DEVICE
+    assert L.forge_dgrad(FAKE, FAKE, FAKE, 64, 64, 64, fg.FORGE_BF16, None) == \
+        fg.FORGE_ERR_UNSUPPORTED_DEVICE
     assert fg.forge_get_device_status() == fg.FORGE_ERR_UNSUPPORTED_DEVICE

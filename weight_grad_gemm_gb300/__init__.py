@@ -34,7 +34,7 @@ FORGE_E4M3 = 1
 FORGE_F32 = 2
 
 EXPORTS = ("forge_wgrad_adamw", "forge_wgrad_adamw_noalloc", "forge_wgrad_sgdm", "forge_wgrad_only",
-           "forge_quantize_e4m3",
+           "forge_quantize_e4m3", "forge_dgrad", "forge_backward_adamw",
            "forge_grouped_wgrad_adamw", "forge_status_string", "forge_get_device_status",
            "forge_selftest_wait_timeout", "forge_version")
 
@@ -61,12 +61,15 @@ def lib() -> ctypes.CDLL:
     L.forge_wgrad_adamw.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, F, F, F, F, F, I64, P, P]
     L.forge_wgrad_adamw_noalloc.argtypes = L.forge_wgrad_adamw.argtypes
     L.forge_quantize_e4m3.argtypes = [P, I, I64, P, P, P]
+    L.forge_dgrad.argtypes = [P, P, P, I64, I64, I64, I, P]
+    L.forge_backward_adamw.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I, I, F, F, F, F, F,
+                                       I64, P]
     L.forge_wgrad_sgdm.argtypes = [P, P, P, P, I64, I64, I64, I, I, F, F, F, P, P]
     L.forge_wgrad_only.argtypes = [P, P, P, I64, I64, I64, I, P, P]
     L.forge_grouped_wgrad_adamw.argtypes = [P, P, P, P, P, P, I32, I64, I64, I64, I, I, F, F, F,
                                             F, F, I64, P, P]
     for f in ("forge_wgrad_adamw", "forge_wgrad_adamw_noalloc", "forge_wgrad_sgdm",
-              "forge_wgrad_only", "forge_quantize_e4m3",
+              "forge_wgrad_only", "forge_quantize_e4m3", "forge_dgrad", "forge_backward_adamw",
               "forge_grouped_wgrad_adamw", "forge_get_device_status",
               "forge_selftest_wait_timeout"):
         getattr(L, f).restype = I
@@ -191,6 +194,37 @@ def forge_quantize_e4m3(x, codes, scale, *, stream=None):
     s = lib().forge_quantize_e4m3(_ptr(x), _dtype_code(x), x.numel(), _ptr(codes), _ptr(scale),
                                   _stream(stream, codes))
     _check(s, "forge_quantize_e4m3")
+
+
+def forge_dgrad(dY, Wb, dX, *, stream=None):
+    """dX [K, N] (bf16) = dY [K, M] (bf16) times Wb [N, M] (bf16) transposed."""
+    K, M = dY.shape
+    N = Wb.shape[0]
+    if Wb.dim() != 2 or Wb.shape[1] != M or tuple(dX.shape) != (K, N):
+        raise ValueError(f"dY [K, M], Wb [N, M], dX [K, N] expected, got {tuple(dY.shape)}, "
+                         f"{tuple(Wb.shape)}, {tuple(dX.shape)}")
+    s = lib().forge_dgrad(_ptr(dY), _ptr(Wb), _ptr(dX), M, N, K, _dtype_code(dY),
+                          _stream(stream, dX))
+    _check(s, "forge_dgrad")
+
+
+def forge_backward_adamw(X, dY, W, m, v, dX, *, lr, beta1, beta2, eps, wd, step, Wb=None,
+                         stream=None):
+    """dX = dY Wb^T, then the fused dW + AdamW on W, m, v, in that order on one
+    stream.  Wb: the bf16 copy of W the forward used, or None to have W
+    rounded to bf16 first."""
+    M, N, K = _sizes(X, dY)
+    for t in (W, m, v):
+        if tuple(t.shape) != (N, M):
+            raise ValueError(f"W/m/v must be [N={N}, M={M}], got {tuple(t.shape)}")
+    if tuple(dX.shape) != (K, N) or (Wb is not None and tuple(Wb.shape) != (N, M)):
+        raise ValueError("dX must be [K, N] and Wb [N, M]")
+    if m.dtype != v.dtype:
+        raise TypeError("m and v must share a dtype")
+    s = lib().forge_backward_adamw(_ptr(X), _ptr(dY), _ptr(W), _ptr(m), _ptr(v), _ptr(Wb),
+                                   _ptr(dX), M, N, K, _dtype_code(X), _dtype_code(m), lr, beta1,
+                                   beta2, eps, wd, int(step), _stream(stream, W))
+    _check(s, "forge_backward_adamw")
 
 
 def forge_grouped_wgrad_adamw(X, dY, W, m, v, offsets, *, lr, beta1, beta2, eps, wd, step,

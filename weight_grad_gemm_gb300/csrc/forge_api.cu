@@ -103,8 +103,8 @@ forge_status current_device(DeviceInfo** out)
 // multiple of 16) -> TMA map with 128-byte swizzled boxes of (128 bytes of
 // the inner dimension) x (k rows per stage / row_split).  row_split = 0 asks
 // for one-row boxes, the form tile::gather4 copies use.
-forge_status encode_operand(CUtensorMap* map, const void* base, forge_dtype dt, int64_t inner,
-                            int64_t rows, int64_t ld_bytes, int row_split = 1)
+// Resolves cuTensorMapEncodeTiled through the runtime once per process.
+bool ensure_encode()
 {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
@@ -116,7 +116,13 @@ forge_status encode_operand(CUtensorMap* map, const void* base, forge_dtype dt, 
         else
             cudaGetLastError();
     });
-    if (!g_encode) return FORGE_ERR_CUDA;
+    return g_encode != nullptr;
+}
+
+forge_status encode_operand(CUtensorMap* map, const void* base, forge_dtype dt, int64_t inner,
+                            int64_t rows, int64_t ld_bytes, int row_split = 1)
+{
+    if (!ensure_encode()) return FORGE_ERR_CUDA;
     const int es = elem_size(dt);
     const cuuint32_t box_inner = 128 / es;
     const cuuint32_t box_rows =
@@ -497,6 +503,46 @@ forge_status forge::device_sms(int* sms)
     const forge_status st = current_device(&dev);
     if (st == FORGE_OK) *sms = dev->sms;
     return st;
+}
+
+int* forge::device_status_word()
+{
+    DeviceInfo* dev = nullptr;
+    return current_device(&dev) == FORGE_OK ? dev->status : nullptr;
+}
+
+int64_t forge::wait_timeout() { return wait_timeout_ns(); }
+
+cudaError_t forge::encode_bf16_kmajor(CUtensorMap* map, const void* base, int64_t inner,
+                                      int64_t rows, uint32_t box_rows)
+{
+    if (!ensure_encode()) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r =
+        g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+forge_status forge::adamw_checks(const void* X, const void* dY, const float* W, const void* m,
+                                 const void* v, int64_t M, int64_t N, int64_t K,
+                                 forge_dtype in_dtype, forge_dtype state_dtype, float lr,
+                                 float beta1, float beta2, float eps, float wd, int64_t step)
+{
+    if (!W || !m || !v) return FORGE_ERR_INVALID_ARG;
+    forge_status s;
+    if ((s = check_sizes(M, N, K)) != FORGE_OK) return s;
+    if ((s = check_inputs(X, dY, K, in_dtype, nullptr)) != FORGE_OK) return s;
+    if (state_dtype != FORGE_F32 && state_dtype != FORGE_BF16) return FORGE_ERR_UNSUPPORTED_DTYPE;
+    if ((s = check_adam(lr, beta1, beta2, eps, wd, step)) != FORGE_OK) return s;
+    const uintptr_t sa = state_dtype == FORGE_BF16 ? 2 : 4;
+    if (!aligned(W, 4) || !aligned(m, sa) || !aligned(v, sa)) return FORGE_ERR_MISALIGNED;
+    if (K > 0 && operand_path(X, N, elem_size(in_dtype)) < 0) return FORGE_ERR_MISALIGNED;
+    return FORGE_OK;
 }
 
 extern "C" {

@@ -1,6 +1,12 @@
-// forge_device.h -- the device check every entry point makes (defined in
-// forge_api.cu).
+// forge_device.h -- host helpers shared by the entry points (defined in
+// forge_api.cu): the device check, the device status word, the bounded-wait
+// limit, TMA descriptor encoding and the AdamW argument checks.
 #pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
 #include "forge.h"
 
 namespace forge {
@@ -8,5 +14,25 @@ namespace forge {
 // The current device, checked once per device for compute capability 10.3;
 // on success *sms receives its SM count.
 forge_status device_sms(int* sms);
+
+// Device address of the status word on the current device (after a
+// successful device_sms call).
+int* device_status_word();
+
+// Bounded-wait limit in nanoseconds (FORGE_WAIT_TIMEOUT_MS, default 10 s).
+int64_t wait_timeout();
+
+// bf16 [rows, inner] row-major, 16-byte aligned base and row stride, read in
+// boxes of 64 elements of the inner (contraction) dimension x box_rows rows
+// with 128-byte swizzle: the K-major operand layout of tcgen05.mma.
+cudaError_t encode_bf16_kmajor(CUtensorMap* map, const void* base, int64_t inner, int64_t rows,
+                               uint32_t box_rows);
+
+// The host-side checks forge_wgrad_adamw makes before any launch, including
+// the alignment of X, W, m and v (dY is the caller's to check).
+forge_status adamw_checks(const void* X, const void* dY, const float* W, const void* m,
+                          const void* v, int64_t M, int64_t N, int64_t K, forge_dtype in_dtype,
+                          forge_dtype state_dtype, float lr, float beta1, float beta2, float eps,
+                          float wd, int64_t step);
 
 }  // namespace forge

@@ -1,0 +1,380 @@
+// forge_dgrad.cu -- the input gradient dX = dY W^T, and the backward step that
+// orders it before the in-place weight update.
+//
+// "Math verified, not asserted", P1: the fused update overwrites W in place,
+// so dX must have read W first (FORGE's in-place dX-before-update hazard).
+// forge_backward_adamw issues both on one stream in that order, so the caller
+// no longer has to.
+//
+// The contraction here runs over d_out (M): dX[k][n] = sum_m dY[k][m] W[n][m].
+// Both operands keep the contraction index contiguous (dY rows, W rows), so
+// both are K-major for the tensor core: TMA boxes of 64 bf16 of d_out (one
+// 128-byte swizzle row) x 128 token rows (A) or x 256 weight rows (B).  One
+// CTA per SM, persistent over 128 (tokens) x 256 (d_in) output tiles ordered
+// token-fastest, so a wave of tiles shares W's rows in L2 while dY streams;
+// warp 0 is the TMA producer, lane 0 of warp 1 the MMA issuer, warps 4-11 the
+// epilogue (TMEM -> fp32 -> bf16, nearest even, 32-byte row segments per
+// lane).  The accumulator is double-buffered in TMEM (2 x 256 columns).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "forge.h"
+#include "forge_device.h"
+#include "forge_kernel.cuh"
+
+namespace forge {
+namespace dgrad {
+
+constexpr int BT = 128;  // tokens per tile: UMMA M, TMEM lanes
+constexpr int BN = 256;  // d_in per tile: UMMA N, TMEM columns per accumulator
+constexpr int BK = 64;   // d_out per stage: one 128-byte swizzle row of bf16
+constexpr int UK = 16;   // d_out per MMA instruction (kind::f16)
+constexpr int kStages = 4;
+constexpr int kStageA = BT * BK * 2;  // 16 KB
+constexpr int kStageB = BN * BK * 2;  // 32 KB
+constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kSmemBar = kStages * kStageBytes;
+constexpr int kSmemBytes = kSmemBar + 256;
+constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdesc = ptx::make_idesc(1, 1, false, false, BT, BN);  // bf16, K-major
+
+struct DParams {
+    int64_t K, N, M;
+    int32_t tiles_t, tiles_n;
+    __nv_bfloat16* dX;
+    int32_t vec_ok;  // N % 8 == 0 and dX 16-byte aligned: 16-byte stores
+    Params w;        // timeout_ns and status for the bounded waits
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    forge_dgrad_kernel(const __grid_constant__ CUtensorMap tmA,  // dY [K, M]
+                       const __grid_constant__ CUtensorMap tmB,  // W  [N, M]
+                       const DParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemBar);
+    uint64_t* empty = full + kStages;
+    uint64_t* tfull = empty + kStages;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&tfull[b], 1);
+            ptx::mbar_init(&tempty[b], kEpiWarps);
+        }
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0;
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(tmem_slot, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int32_t total = p.tiles_t * p.tiles_n;
+    const int32_t nk = static_cast<int32_t>((p.M + BK - 1) / BK);
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued_mask = 0, last_parity = 0;
+            bool ok = true;
+            for (int32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const int32_t t0 = (t % p.tiles_t) * BT;
+                const int32_t n0 = (t / p.tiles_t) * BN;
+                for (int32_t kb = 0; kb < nk; ++kb) {
+                    if (!wait_bounded(&empty[s], ph ^ 1u, abort_flag, p.w)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&full[s], kStageBytes);
+                    uint8_t* sa = smem + s * kStageBytes;
+                    ptx::tma_load_2d(sa, &tmA, &full[s], kb * BK, t0);
+                    ptx::tma_load_2d(sa + kStageA, &tmB, &full[s], kb * BK, n0);
+                    issued_mask |= 1u << s;
+                    last_parity = (last_parity & ~(1u << s)) | (ph << s);
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // wait (bounded) for this thread's copies still in flight
+                const uint64_t tw = ptx::globaltimer_ns();
+                for (int q = 0; q < kStages; ++q) {
+                    if (!(issued_mask & (1u << q))) continue;
+                    const uint32_t a = ptx::smem_addr(&full[q]);
+                    while (!ptx::mbar_try_wait(a, (last_parity >> q) & 1u)) {
+                        if (static_cast<int64_t>(ptx::globaltimer_ns() - tw) > p.w.timeout_ns)
+                            break;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------- MMA issuer (lane 0)
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t ct = 0;
+            bool ok = true;
+            bool issued_any = false;
+            for (int32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const uint32_t b = ct & 1u;
+                ok = wait_bounded(&tempty[b], ((ct >> 1) & 1u) ^ 1u, abort_flag, p.w);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + b * BN;
+                for (int32_t kb = 0; kb < nk; ++kb) {
+                    ok = wait_bounded(&full[s], ph, abort_flag, p.w);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_addr(smem + s * kStageBytes);
+                    const uint32_t sb = sa + kStageA;
+#pragma unroll
+                    for (int ks = 0; ks < BK / UK; ++ks) {
+                        // K-major, 128-byte swizzle: 8-row groups 1024 bytes apart;
+                        // the k sub-block is a 32-byte step inside the swizzle row
+                        const uint64_t ad = ptx::smem_desc_sw128(sa + ks * UK * 2, 16, 1024);
+                        const uint64_t bd = ptx::smem_desc_sw128(sb + ks * UK * 2, 16, 1024);
+                        ptx::umma_f16(d_tmem, ad, bd, kIdesc, (kb | ks) != 0 ? 1u : 0u);
+                    }
+                    ptx::umma_commit(&empty[s]);
+                    issued_any = true;
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::umma_commit(&tfull[b]);
+                ++ct;
+            }
+            if (!ok && issued_any) {
+                ptx::umma_commit(drain);
+                const uint32_t a = ptx::smem_addr(drain);
+                const uint64_t tw = ptx::globaltimer_ns();
+                while (!ptx::mbar_try_wait(a, 0)) {
+                    if (static_cast<int64_t>(ptx::globaltimer_ns() - tw) > p.w.timeout_ns) break;
+                }
+            }
+        }
+    } else if (warp >= kEpiWarp0) {
+        // ---------------------------------------------------- epilogue
+        // Warp (q, half): TMEM lanes 32q.. (tokens) x columns 128 half .. (d_in),
+        // in 16-column chunks; each lane stores its own row's 32 bytes.
+        const int q = warp & 3;
+        const int half = (warp - kEpiWarp0) >> 2;
+        uint32_t ct = 0;
+        for (int32_t t = blockIdx.x; t < total; t += gridDim.x) {
+            const uint32_t b = ct & 1u;
+            if (!warp_wait(&tfull[b], (ct >> 1) & 1u, abort_flag, p.w, lane)) break;
+            ptx::tc_fence_after();
+            const int64_t row = static_cast<int64_t>(t % p.tiles_t) * BT + 32 * q + lane;
+            const int64_t cbase = static_cast<int64_t>(t / p.tiles_t) * BN + 128 * half;
+            const uint32_t tcol =
+                tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN + 128 * half;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+                uint32_t r[16];
+                ptx::tmem_ld_32x32b_x16(tcol + 16 * c, r);
+                ptx::tmem_ld_wait();
+                if (c == 7) {  // accumulator fully read
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&tempty[b]);
+                }
+                const int64_t col0 = cbase + 16 * c;
+                if (row >= p.K || col0 >= p.N) continue;
+                __nv_bfloat16* dst = p.dX + row * p.N + col0;
+                if (p.vec_ok && col0 + 16 <= p.N) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(
+                            __uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                        w[j] = *reinterpret_cast<const uint32_t*>(&h);
+                    }
+                    reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (col0 + j < p.N) dst[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+                }
+            }
+            ++ct;
+            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// fp32 -> bf16, nearest even: the bf16 copy of W the input gradient reads
+// when the caller has none.
+__global__ void __launch_bounds__(256) forge_round_bf16_kernel(const float* __restrict__ src,
+                                                               __nv_bfloat16* __restrict__ dst,
+                                                               int64_t n)
+{
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += stride)
+        dst[i] = __float2bfloat16_rn(__ldcs(src + i));
+}
+
+bool aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+cudaError_t launch(const void* dY, const void* Wb, void* dX, int64_t M, int64_t N, int64_t K,
+                   int sms, cudaStream_t stream)
+{
+    CUtensorMap ta, tb;
+    if (encode_bf16_kmajor(&ta, dY, M, K, BT) != cudaSuccess ||
+        encode_bf16_kmajor(&tb, Wb, M, N, BN) != cudaSuccess)
+        return cudaErrorInvalidValue;
+    DParams p{};
+    p.K = K;
+    p.N = N;
+    p.M = M;
+    p.tiles_t = static_cast<int32_t>((K + BT - 1) / BT);
+    p.tiles_n = static_cast<int32_t>((N + BN - 1) / BN);
+    p.dX = static_cast<__nv_bfloat16*>(dX);
+    p.vec_ok = (N % 8 == 0) && aligned(dX, 16);
+    p.w.timeout_ns = wait_timeout();
+    p.w.status = device_status_word();
+    static unsigned long long attr_done = 0;  // one bit per device ordinal < 64
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
+        e = cudaFuncSetAttribute(forge_dgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);
+    }
+    const int64_t total = static_cast<int64_t>(p.tiles_t) * p.tiles_n;
+    const int grid = static_cast<int>(total < sms ? total : sms);
+    forge_dgrad_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+// Host checks of the input-gradient call.  Wb may be NULL only where the
+// caller lets the library round W itself (wb_optional).
+forge_status check(const void* dY, const void* Wb, const void* dX, int64_t M, int64_t N,
+                   int64_t K, forge_dtype in_dtype, bool wb_optional)
+{
+    if (M < 1 || N < 1 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return FORGE_ERR_INVALID_ARG;
+    if (K > 0 && (!dY || !dX)) return FORGE_ERR_INVALID_ARG;
+    if (!Wb && !wb_optional) return FORGE_ERR_INVALID_ARG;
+    if (in_dtype != FORGE_BF16) return FORGE_ERR_UNSUPPORTED_DTYPE;
+    // TMA reads dY and W rows: 16-byte aligned bases and row strides
+    if ((Wb && !aligned(Wb, 16)) || (dY && !aligned(dY, 16)) || (M * 2) % 16 != 0 ||
+        (dX && !aligned(dX, 2)))
+        return FORGE_ERR_MISALIGNED;
+    return FORGE_OK;
+}
+
+}  // namespace dgrad
+}  // namespace forge
+
+using namespace forge;
+
+extern "C" forge_status forge_dgrad(const void* dY, const void* Wb, void* dX, int64_t M,
+                                    int64_t N, int64_t K, forge_dtype in_dtype,
+                                    forge_stream_t stream)
+{
+    forge_status st = dgrad::check(dY, Wb, dX, M, N, K, in_dtype, false);
+    if (st != FORGE_OK) return st;
+    int sms = 0;
+    if ((st = device_sms(&sms)) != FORGE_OK) return st;
+    if (K == 0) return FORGE_OK;
+    return dgrad::launch(dY, Wb, dX, M, N, K, sms, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? FORGE_OK
+               : FORGE_ERR_CUDA;
+}
+
+extern "C" forge_status forge_backward_adamw(const void* X, const void* dY, float* W, void* m,
+                                             void* v, const void* Wb, void* dX, int64_t M,
+                                             int64_t N, int64_t K, forge_dtype in_dtype,
+                                             forge_dtype state_dtype, float lr, float beta1,
+                                             float beta2, float eps, float wd, int64_t step,
+                                             forge_stream_t stream)
+{
+    // every check of both halves runs before the first launch
+    forge_status st = dgrad::check(dY, Wb, dX, M, N, K, in_dtype, true);
+    if (st != FORGE_OK) return st;
+    if ((st = adamw_checks(X, dY, W, m, v, M, N, K, in_dtype, state_dtype, lr, beta1, beta2, eps,
+                           wd, step)) != FORGE_OK)
+        return st;
+    // the weight copy the input gradient reads: the caller's, or W rounded now
+    const void* wb = Wb;
+    int sms = 0;
+    if ((st = device_sms(&sms)) != FORGE_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void* scratch = nullptr;
+    if (K > 0) {
+        if (!Wb) {
+            const int64_t n = N * M;
+            if (cudaMallocAsync(&scratch, static_cast<size_t>(n) * 2, s) != cudaSuccess) {
+                cudaGetLastError();
+                return FORGE_ERR_CUDA;
+            }
+            const int64_t want = (n + 255) / 256;
+            const int blocks = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);
+            dgrad::forge_round_bf16_kernel<<<blocks, 256, 0, s>>>(
+                W, static_cast<__nv_bfloat16*>(scratch), n);
+            wb = scratch;
+        }
+        // dX from the weights as they are before this step's update ...
+        cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess) e = dgrad::launch(dY, wb, dX, M, N, K, sms, s);
+        if (scratch) {
+            const cudaError_t fe = cudaFreeAsync(scratch, s);
+            if (e == cudaSuccess) e = fe;
+        }
+        if (e != cudaSuccess) return FORGE_ERR_CUDA;
+    }
+    // ... then the fused dW + AdamW that overwrites W, later on the same stream
+    return forge_wgrad_adamw(X, dY, W, m, v, M, N, K, in_dtype, state_dtype, lr, beta1, beta2, eps,
+                             wd, step, nullptr, stream);
+}
