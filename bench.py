@@ -556,6 +556,26 @@ def run_reference(args):
     return 0
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x (the slowest rank's time); x itself on
+    one rank.  Works on any initialised process group (NCCL with a CUDA
+    device, gloo with the CPU)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(flops_per_rank: float, world: int, ms: float) -> float:
+    """TFLOP/s of the whole job: every replica does flops_per_rank per step,
+    and the step takes the slowest rank's ms."""
+    return flops_per_rank * world / (ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- our arm
 
 def main():
@@ -628,14 +648,9 @@ def main():
         raise RuntimeError("device status not OK after the timed region")
 
     per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = float(sum(per_step_ms))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(per_step_ms)), world, dev)
     ms = total_ms / args.steps
-    value = job.flops * world / (ms * 1e-3) / 1e12
+    value = whole_job_rate(job.flops, world, ms)
 
     # end to end through the C ABI with pinned host buffers: this step's
     # inputs are copied in and the updated parameters copied out, every step
@@ -660,12 +675,7 @@ def main():
         b.synchronize()
         if i >= 2:
             e2e_times.append(a.elapsed_time(b))
-    e2e_ms = float(np.mean(e2e_times)) if e2e_times else float("nan")
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(float(np.mean(e2e_times)) if e2e_times else float("nan"), world, dev)
     h2d = sum(h.numel() * h.element_size() for h in ins_h)
     d2h = res_h.numel() * res_h.element_size()
 
@@ -700,7 +710,7 @@ def main():
         "roofline": {"bound": "tensor" if t_tensor >= t_hbm else "hbm", "achieved": kernel_tf,
                      "peak": peak_tf, "unit": "TFLOP/s", "frac": kernel_tf / peak_tf,
                      "peak_source": peak_note, "traffic": traffic},
-        "e2e": {"value": job.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": whole_job_rate(job.flops, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * getattr(job, "launches", 1) if args.impl == "ours" else 0,
         "clocks": clk,
