@@ -406,7 +406,9 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, 
             if (lane == 0) release_acc(b);
         };
 
-        auto fetch = [&](int c, Chunk& ch) {
+        // The gradient of chunk c: TMEM -> registers -> stage -> this lane's
+        // 4 m x chunk_n n (zeros for a tile without tokens).
+        auto grad = [&](int c, Chunk& ch) {
             if (has_acc) {
                 uint32_t r[kChunkCols];
                 tmem_ld_chunk(tcol + kChunkCols * c, r);
@@ -430,6 +432,9 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, 
 #pragma unroll
                 for (int j = 0; j < 4 * kChunkN; ++j) ch.g[j] = 0.0f;
             }
+        };
+        // The state loads of chunk c.
+        auto state = [&](int c, Chunk& ch) {
             if constexpr (OP != OP_DW) {
 #pragma unroll
                 for (int jj = 0; jj < kChunkN; ++jj) {
@@ -496,15 +501,28 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, 
         if (nchunks == 0) {
             if (has_acc) release();
         } else {
+            // Early: a chunk's gradient is read with its state loads, so the
+            // TMEM latency overlaps them.  Late (sixteen warps, 96 registers):
+            // the gradient is read just before the update, which keeps one
+            // chunk's gradient fewer live and the epilogue free of spills.
+            constexpr bool kLateGrad = EC::warps == 16;
+            auto fetch = [&](int c, Chunk& ch) {
+                if constexpr (!kLateGrad) grad(c, ch);
+                state(c, ch);
+            };
+            auto update = [&](int c, Chunk& ch) {
+                if constexpr (kLateGrad) grad(c, ch);
+                process(c, ch);
+            };
             Chunk A, B;
             fetch(0, A);
 #pragma unroll 1
             for (int c = 0; c < nchunks; c += 2) {
                 if (c + 1 < nchunks) fetch(c + 1, B);
-                process(c, A);
+                update(c, A);
                 if (c + 1 < nchunks) {
                     if (c + 2 < nchunks) fetch(c + 2, A);
-                    process(c + 1, B);
+                    update(c + 1, B);
                 }
             }
         }
