@@ -31,6 +31,13 @@ def check_dx(got_bf16, exact):
     assert bad[0].size == 0, (bad[0][:5], got[bad][:5], exact[bad][:5])
 
 
+@pytest.fixture(params=["single", "pair"])
+def dgrad_form(request, monkeypatch):
+    """Run on the one-CTA kernel and on CTA pairs."""
+    monkeypatch.setenv("FORGE_DGRAD_KERNEL", request.param)
+    return request.param
+
+
 def inputs(K, N, M, seed, dev):
     D = wl.activations(K, M, wl.seed_of("dg-dY", seed, K, M), device=dev)
     Wb = wl.randn((N, M), wl.seed_of("dg-W", seed, N, M), device=dev, std=0.02).to(torch.bfloat16)
@@ -39,7 +46,7 @@ def inputs(K, N, M, seed, dev):
 
 @pytest.mark.parametrize("K,N,M", [(200, 520, 296), (1, 8, 8), (129, 257, 64),
                                    (1000, 1032, 648), (300, 250, 4104), (64, 256, 128)])
-def test_dgrad_matches_oracle(cuda_device, K, N, M):
+def test_dgrad_matches_oracle(cuda_device, dgrad_form, K, N, M):
     D, Wb = inputs(K, N, M, 1, cuda_device)
     dX = torch.full((K, N), float("nan"), dtype=torch.bfloat16, device=cuda_device)
     fg.forge_dgrad(D, Wb, dX)
@@ -60,20 +67,20 @@ def test_dgrad_no_tokens_and_misaligned_rows(cuda_device):
     assert e.value.status == fg.FORGE_ERR_MISALIGNED
 
 
-def test_dgrad_full_size_sampled_rows(cuda_device):
+def test_dgrad_full_size_sampled_rows(cuda_device, dgrad_form):
     wk = wl.MLP_DOWN
     K, N, M = wk.K, wk.N, wk.M
     D, Wb = inputs(K, N, M, 4, cuda_device)
     dX = torch.empty((K, N), dtype=torch.bfloat16, device=cuda_device)
     fg.forge_dgrad(D, Wb, dX)
     torch.cuda.synchronize()
-    rows = [0, 127, 128, K // 2, K - 1]
+    rows = [0, 127, 128, 255, 256, K // 2, K - 1]
     exact = oracle.dgrad(oracle.as_bits(D.cpu()), oracle.as_bits(Wb.cpu()), rows=rows)
     check_dx(dX[rows], exact)
 
 
 @pytest.mark.parametrize("given_copy", [True, False], ids=["Wb", "rounded"])
-def test_backward_reads_weights_before_the_update(cuda_device, given_copy):
+def test_backward_reads_weights_before_the_update(cuda_device, dgrad_form, given_copy):
     """forge_backward_adamw = forge_dgrad on the pre-update bf16 weights, then
     forge_wgrad_adamw: both halves bit for bit."""
     dev = cuda_device
