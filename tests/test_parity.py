@@ -304,6 +304,19 @@ def test_grouped_single_expert_equals_dense_bitwise(cuda_device, grouped_form):
         assert np.array_equal(a[0], b)
 
 
+def test_grouped_many_experts(cuda_device, grouped_form):
+    """257 experts, a third of them without tokens, ragged counts: the
+    offset copy, validation and heavy-first ranking run over every expert."""
+    rng = np.random.default_rng(24)
+    counts = rng.integers(0, 40, size=257)
+    counts[rng.random(257) < 0.33] = 0
+    N, M = 136, 264
+    X, D, off, W, m, v, sc = grouped_case(list(counts), N, M, 25)
+    got = run_grouped(cuda_device, X, D, off, W, m, v, step=4)
+    assert fg.forge_get_device_status() == fg.FORGE_OK
+    check_grouped(got, X, D, off, W, m, v, 4, sc, False)
+
+
 def test_grouped_foreign_tokens_never_enter(cuda_device, grouped_form):
     """Expert e's gradient is the sum over its own tokens only: non-finite
     values in a neighbour's rows (which share the partial k-blocks at both

@@ -93,11 +93,13 @@ def test_attention_projections_full_size(cuda_device, idx, state):
               torch.float32 if state == "f32" else torch.bfloat16, step=2)
 
 
-def test_moe_grouped_full_size(cuda_device):
+@pytest.mark.parametrize("state", ["f32", "bf16"])
+def test_moe_grouped_full_size(cuda_device, state):
     """8 experts of [14336, 4096]; step 2 of the routed workload, on which 4
     seeded experts receive no tokens (their m, v decay exactly by beta)."""
     wk = wl.MOE
     dev = cuda_device
+    sdt = torch.float32 if state == "f32" else torch.bfloat16
     E, N, M = wk.experts, wk.N, wk.M
     step = 2
     zero = wl.moe_zero_experts(wl.seed_of(wk.name, "zero", step), E)
@@ -111,8 +113,8 @@ def test_moe_grouped_full_size(cuda_device):
     hp = wk.adam.f32()
     # step 1 (all experts routed) warms the state from zero with the library
     W = wl.randn((E, N, M), wl.seed_of(wk.name, "W"), device=dev, std=0.02)
-    m = torch.zeros((E, N, M), device=dev)
-    v = torch.zeros((E, N, M), device=dev)
+    m = torch.zeros((E, N, M), device=dev, dtype=sdt)
+    v = torch.zeros((E, N, M), device=dev, dtype=sdt)
     c1 = wl.zipf_top2_counts(wl.seed_of(wk.name, "route", 1), tokens=16384, experts=E)
     off1 = torch.from_numpy(wl.offsets_from_counts(c1).astype(np.int32)).to(dev)
     fg.forge_grouped_wgrad_adamw(wl.activations(T, N, wl.seed_of(wk.name, "X", 1), device=dev),
@@ -131,9 +133,12 @@ def test_moe_grouped_full_size(cuda_device):
     for e in range(E):
         G = oracle.wgrad(Xh, Dh, rows=rows, k_range=(int(off[e]), int(off[e + 1])))
         ref = oracle.adamw(G, W0[e], m0[e], v0[e], step=step, **vars(hp))
-        check_rows(W1[e], m1[e], v1[e], ref, G, hp.lr, False, m0=m0[e], beta1=hp.beta1)
-        if counts[e] == 0:
-            # g = 0: m' = RN(b1 m), v' = RN(b2 v) exactly, as the oracle rounds them
+        check_rows(W1[e], m1[e], v1[e], ref, G, hp.lr, state == "bf16", m0=m0[e],
+                   beta1=hp.beta1)
+        if counts[e] == 0 and state == "f32":
+            # g = 0: m' = RN(b1 m), v' = RN(b2 v) exactly, as the oracle rounds
+            # them (with bf16 state the fp32 product is rounded again to bf16,
+            # which the band check above covers)
             assert np.array_equal(m1[e], ref["m"]) and np.array_equal(v1[e], ref["v"])
 
 
