@@ -687,6 +687,7 @@ def main():
         peak_tf = peaks["bf16_tflops"] * 2.0
         peak_note = f"bf16_tflops burst x 2 (nominal fp8/bf16), {peak_src}"
     bw = peaks["hbm_gbs"]
+    sustained_ratio = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) / peaks["bf16_tflops"]
     kernel_tf = job.flops / (ms * 1e-3) / 1e12
     t_tensor = job.flops / (peak_tf * 1e12)
     t_hbm = job.bytes / (bw * 1e9)
@@ -709,7 +710,9 @@ def main():
         "grad_w_hbm_bytes": gradw,
         "roofline": {"bound": "tensor" if t_tensor >= t_hbm else "hbm", "achieved": kernel_tf,
                      "peak": peak_tf, "unit": "TFLOP/s", "frac": kernel_tf / peak_tf,
-                     "peak_source": peak_note, "traffic": traffic},
+                     "peak_source": peak_note, "traffic": traffic,
+                     # the same against the power-capped (seconds-long) cuBLAS rate
+                     "frac_sustained": kernel_tf / (peak_tf * sustained_ratio)},
         "e2e": {"value": whole_job_rate(job.flops, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * getattr(job, "launches", 1) if args.impl == "ours" else 0,
