@@ -41,10 +41,11 @@
  * scratch per call and forge_backward_adamw without a bf16 weight copy takes
  * one (see there), and an operand (X or dY) whose base is not
  * 16-byte aligned or whose row stride is not a multiple of 16 bytes is first
- * copied into a padded scratch buffer taken from the device's default memory
- * pool with cudaMallocAsync on `stream` and returned with cudaFreeAsync on
- * the same stream after the kernel (one extra read and write of that
- * operand).  If that allocation fails, or the environment variable
+ * copied into a padded scratch buffer, allocated in stream order on `stream`
+ * from a memory pool the library creates per device and freed in stream
+ * order after the kernel (one extra read and write of that operand).  The
+ * pool keeps the memory it has reserved for later calls (at most the largest
+ * scratch in use at once) until the process ends.  If that allocation fails, or the environment variable
  * FORGE_MISALIGNED is "loader", the kernel fetches such an operand itself
  * with cp.async instead.  W, m, v, buf are updated in place.  Calls are asynchronous and
  * ordered on `stream`; the return value reports only host-side validation
@@ -171,9 +172,8 @@ FORGE_API forge_status forge_wgrad_adamw_noalloc(const void* X, const void* dY, 
  *           out of the amax (their codes are NaN).
  * Pass codes and scale as X (or dY) and scales[0] (or scales[1]) of an e4m3
  * call.  Two passes over x: the first writes one partial maximum per block
- * (at most four blocks per SM) into a scratch array taken from the device's
- * default memory pool with cudaMallocAsync on `stream`, returned with
- * cudaFreeAsync after the second.  Errors: n < 0, scale NULL, or x / codes
+ * (at most four blocks per SM) into a scratch array from the library's memory
+ * pool, allocated and freed in stream order on `stream`.  Errors: n < 0, scale NULL, or x / codes
  * NULL with n > 0 -> FORGE_ERR_INVALID_ARG; x_dtype -> FORGE_ERR_UNSUPPORTED_DTYPE;
  * x not aligned to its element size or scale not 4-byte aligned ->
  * FORGE_ERR_MISALIGNED.
@@ -203,8 +203,8 @@ FORGE_API forge_status forge_dgrad(const void* dY, const void* Wb, void* dX, int
  * W, m, v (exactly forge_wgrad_adamw), both on `stream`, so dX always sees
  * the weights from before this step.  Wb is the bf16 copy of W the forward
  * pass used; with Wb == NULL the library first rounds W to bf16 (nearest
- * even) into a stream-ordered scratch copy (N * M * 2 bytes, cudaMallocAsync
- * / cudaFreeAsync on `stream`).  bf16 inputs only.  Every argument check of
+ * even) into a scratch copy (N * M * 2 bytes) from its memory pool, allocated
+ * and freed in stream order on `stream`.  bf16 inputs only.  Every argument check of
  * both halves runs before the first launch; the arguments are those of
  * forge_dgrad and forge_wgrad_adamw.
  */

@@ -7,7 +7,7 @@
 // below (once per device) and, once forge_wgrad_adamw_noalloc has run on a
 // device, its fixed staging buffer; the one per-call allocation is the
 // staging copy of an operand whose rows TMA cannot address (stream-ordered,
-// freed on the same stream after the kernel).
+// from the library's memory pool, freed on the same stream after the kernel).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -362,7 +362,7 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
                 cudaGetLastError();
                 return FORGE_ERR_CUDA;
             }
-        } else if (cudaMallocAsync(&scratch, static_cast<size_t>(need), stream) == cudaSuccess) {
+        } else if (scratch_alloc(&scratch, static_cast<size_t>(need), stream) == cudaSuccess) {
             stage = scratch;
         } else {
             cudaGetLastError();
@@ -385,7 +385,7 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
                 p.manual_b = 0;
             }
             if (ce != cudaSuccess) {
-                if (scratch) cudaFreeAsync(scratch, stream);
+                if (scratch) scratch_free(scratch, stream);
                 return FORGE_ERR_CUDA;
             }
         }
@@ -407,7 +407,7 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
         if (st == FORGE_OK && grouped && !p.manual_b)
             st = encode_operand(&maps.b1, opB, in_dtype, p.N, rows, ldB, 0);
         if (st != FORGE_OK) {
-            if (scratch) cudaFreeAsync(scratch, stream);
+            if (scratch) scratch_free(scratch, stream);
             return st;
         }
     }
@@ -416,7 +416,7 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
     const int64_t tiles_n = (p.N + BN - 1) / BN;
     const int64_t total = tiles_m * tiles_n * p.E;
     if (total <= 0 || total > INT32_MAX) {
-        if (scratch) cudaFreeAsync(scratch, stream);
+        if (scratch) scratch_free(scratch, stream);
         return FORGE_ERR_INVALID_ARG;
     }
     p.tiles_m = static_cast<int32_t>(tiles_m);
@@ -448,7 +448,7 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
     }
     // the staging copy is released after the kernel, in stream order
     if (scratch) {
-        const cudaError_t fe = cudaFreeAsync(scratch, stream);
+        const cudaError_t fe = scratch_free(scratch, stream);
         if (e == cudaSuccess) e = fe;
     }
     return from_cuda(e);
@@ -504,6 +504,42 @@ forge_status forge::device_sms(int* sms)
     if (st == FORGE_OK) *sms = dev->sms;
     return st;
 }
+
+namespace {
+std::mutex g_pool_mu;
+cudaMemPool_t g_pool[kMaxDevices] = {};
+}  // namespace
+
+cudaError_t forge::scratch_alloc(void** ptr, size_t bytes, cudaStream_t stream)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    cudaMemPool_t pool;
+    {
+        std::lock_guard<std::mutex> lk(g_pool_mu);
+        if (!g_pool[dev]) {
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            cudaMemPool_t np;
+            if ((e = cudaMemPoolCreate(&np, &props)) != cudaSuccess) return e;
+            uint64_t keep = ~0ull;
+            if ((e = cudaMemPoolSetAttribute(np, cudaMemPoolAttrReleaseThreshold, &keep)) !=
+                cudaSuccess) {
+                cudaMemPoolDestroy(np);
+                return e;
+            }
+            g_pool[dev] = np;
+        }
+        pool = g_pool[dev];
+    }
+    return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+}
+
+cudaError_t forge::scratch_free(void* ptr, cudaStream_t stream) { return cudaFreeAsync(ptr, stream); }
 
 int* forge::device_status_word()
 {

@@ -28,6 +28,14 @@ int64_t wait_timeout();
 cudaError_t encode_bf16_kmajor(CUtensorMap* map, const void* base, int64_t inner, int64_t rows,
                                uint32_t box_rows);
 
+// Stream-ordered scratch from the library's own memory pool on the current
+// device (created on first use).  The pool keeps what it has reserved (its
+// release threshold is unbounded), so a call after a synchronisation does not
+// map fresh memory again; it holds at most the largest scratch in use at
+// once.  scratch_free returns the block in stream order.
+cudaError_t scratch_alloc(void** ptr, size_t bytes, cudaStream_t stream);
+cudaError_t scratch_free(void* ptr, cudaStream_t stream);
+
 // The host-side checks forge_wgrad_adamw makes before any launch, including
 // the alignment of X, W, m and v (dY is the caller's to check).
 forge_status adamw_checks(const void* X, const void* dY, const float* W, const void* m,

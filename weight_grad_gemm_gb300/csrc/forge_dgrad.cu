@@ -594,7 +594,7 @@ extern "C" forge_status forge_backward_adamw(const void* X, const void* dY, floa
     if (K > 0) {
         if (!Wb) {
             const int64_t n = N * M;
-            if (cudaMallocAsync(&scratch, static_cast<size_t>(n) * 2, s) != cudaSuccess) {
+            if (scratch_alloc(&scratch, static_cast<size_t>(n) * 2, s) != cudaSuccess) {
                 cudaGetLastError();
                 return FORGE_ERR_CUDA;
             }
@@ -608,7 +608,7 @@ extern "C" forge_status forge_backward_adamw(const void* X, const void* dY, floa
         cudaError_t e = cudaGetLastError();
         if (e == cudaSuccess) e = dgrad::launch(dY, wb, dX, M, N, K, sms, s);
         if (scratch) {
-            const cudaError_t fe = cudaFreeAsync(scratch, s);
+            const cudaError_t fe = scratch_free(scratch, s);
             if (e == cudaSuccess) e = fe;
         }
         if (e != cudaSuccess) return FORGE_ERR_CUDA;

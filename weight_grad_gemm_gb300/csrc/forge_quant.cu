@@ -4,7 +4,8 @@
 //
 // Two HBM-bound passes, because no code can be written before amax is known:
 // the first reduces |x| to one partial maximum per block (no atomics: the
-// partials go to a small stream-ordered scratch array), the second has every
+// partials go to a small stream-ordered scratch array from the library's
+// memory pool), the second has every
 // block fold the partials into amax, derive s exactly as the recipe does
 // (amax / 448 divided in fp32), and convert its share of x with the
 // hardware's round-to-nearest-even, saturating fp32 -> e4m3 conversion.
@@ -153,7 +154,7 @@ cudaError_t quantize(const T* x, int64_t n, uint8_t* q, float* scale, int sms,
     cudaError_t e = cudaSuccess;
     const int nparts = n > 0 ? blocks : 0;
     if (nparts > 0) {
-        e = cudaMallocAsync(reinterpret_cast<void**>(&part), nparts * sizeof(float), stream);
+        e = forge::scratch_alloc(reinterpret_cast<void**>(&part), nparts * sizeof(float), stream);
         if (e != cudaSuccess) return e;
         if (vec)
             forge_amax_kernel<T, true><<<blocks, kThreads, 0, stream>>>(x, n, part);
@@ -171,7 +172,7 @@ cudaError_t quantize(const T* x, int64_t n, uint8_t* q, float* scale, int sms,
         e = cudaGetLastError();
     }
     if (part) {
-        const cudaError_t fe = cudaFreeAsync(part, stream);
+        const cudaError_t fe = forge::scratch_free(part, stream);
         if (e == cudaSuccess) e = fe;
     }
     return e;
