@@ -45,10 +45,12 @@
  * from a memory pool the library creates per device and freed in stream
  * order after the kernel (one extra read and write of that operand).  The
  * pool keeps the memory it has reserved for later calls (at most the largest
- * scratch in use at once) until the process ends.  If that allocation fails, or the environment variable
- * FORGE_MISALIGNED is "loader", the kernel fetches such an operand itself
- * with cp.async instead.  W, m, v, buf are updated in place.  Calls are asynchronous and
- * ordered on `stream`; the return value reports only host-side validation
+ * scratch in use at once) until the process ends.  If that allocation fails,
+ * or the environment variable FORGE_MISALIGNED is "loader", the kernel
+ * fetches such an operand itself with cp.async instead.  W, m, v, buf are
+ * updated in place.  Calls are asynchronous and ordered on `stream`, and can
+ * be captured in a CUDA graph once a first call has run on the device; the
+ * return value reports only host-side validation
  * and launch errors.  Errors detected on the device (a bounded wait that
  * ran out) are recorded in a device status word read by
  * forge_get_device_status().

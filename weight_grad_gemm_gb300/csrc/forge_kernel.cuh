@@ -113,7 +113,8 @@ struct Params {
     int32_t has_maps;  // 0 when there are no token rows at all (maps left unencoded)
     int32_t vec_ok;    // M % 4 == 0 and W / state / dW aligned for 4-element vectors
     // Operands whose rows TMA cannot address (row stride or base not a
-    // multiple of 16 bytes) are copied by the cp.async loader instead:
+    // multiple of 16 bytes), when they are not staged into a padded copy,
+    // are copied by the cp.async loader:
     int32_t manual_a, manual_b;  // dY / X loaded by cp.async
     int32_t gran_a, gran_b;      // cp.async width in bytes (4 or 8)
     const uint8_t* gA;           // dY base
