@@ -302,8 +302,8 @@ int operand_path(const void* base, int64_t ld, int es)
     return -1;
 }
 
-// Where a staging copy lives: a stream-ordered allocation from the device's
-// default pool, or the fixed per-device buffer of the no-allocation entry.
+// Where a staging copy lives: a stream-ordered allocation from the library's
+// memory pool, or the fixed per-device buffer of the no-allocation entry.
 enum class StageFrom { Pool, Static };
 
 // Shared tail of every entry point, after the argument checks.
@@ -315,6 +315,10 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
     DeviceInfo* dev = nullptr;
     forge_status st = current_device(&dev);
     if (st != FORGE_OK) return st;
+
+    // the tile list of the smallest tiles must be indexable in 32 bits
+    if (((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN) * p.E > INT32_MAX)
+        return FORGE_ERR_INVALID_ARG;
 
     const int es = elem_size(in_dtype);
     if (rows > 0) {
@@ -414,11 +418,7 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
     const int64_t tile_m = form == 2 ? 4 * BM : (form == 1 ? 2 * BM : BM);
     const int64_t tiles_m = (p.M + tile_m - 1) / tile_m;
     const int64_t tiles_n = (p.N + BN - 1) / BN;
-    const int64_t total = tiles_m * tiles_n * p.E;
-    if (total <= 0 || total > INT32_MAX) {
-        if (scratch) scratch_free(scratch, stream);
-        return FORGE_ERR_INVALID_ARG;
-    }
+    const int64_t total = tiles_m * tiles_n * p.E;  // at least 1, within the bound checked above
     p.tiles_m = static_cast<int32_t>(tiles_m);
     p.tiles_n = static_cast<int32_t>(tiles_n);
     p.raster_band = raster_band(p.tiles_m);
