@@ -52,8 +52,6 @@ constexpr int kStageB = 32768;  // BK rows x 256 n x elemsize
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kTmemCols = 512;  // two 256-column accumulators
 constexpr int kMaxExperts = 1024;
-constexpr int kSmemBarOffset = kStages * kStageBytes;
-constexpr int kSmemSchedOffset = kSmemBarOffset + 256;
 
 // Epilogue geometry for EW epilogue warps.  Warp (q, grp) owns TMEM lane
 // quarter q and warp_cols accumulator columns, walked in chunks of
@@ -80,9 +78,29 @@ constexpr int kStageBytesEpi = 16384;  // the epilogue warps' shared-memory stag
 static_assert(Epi<8>::warps * Epi<8>::stage_floats * 4 == kStageBytesEpi &&
                   Epi<16>::warps * Epi<16>::stage_floats * 4 == kStageBytesEpi,
               "one stage area for both geometries");
-constexpr int kSmemStageOffset = (kSmemSchedOffset + 4 * (2 * kMaxExperts + 2) + 127) & ~127;
-constexpr int kSmemBytes = kSmemStageOffset + kStageBytesEpi;
-constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
+
+// Shared memory of a kernel whose operand ring takes RING bytes: the ring,
+// the mbarriers, the grouped schedule (expert offsets and order) and the
+// epilogue stages.  Shared memory and L1 share 256 KB per SM, and the
+// carve-out is taken in steps (..., 164, 196, 228 KB).  The epilogue's
+// state loads land in L1 while in flight, so with the 228 KB step (a
+// 28 KB L1) an SM keeps too few of them outstanding: a decay-only stream
+// of W, m, v measured 4.5 TB/s there against 6.4 TB/s at the 196 KB step.
+// The CTA-pair kernels (every call with d_out > 128) take a five-stage ring
+// to stay within that step, the 1 KB the runtime keeps per block included.
+// The single-CTA kernel keeps four 48 KB stages and the 228 KB step: with
+// three its MMA starved (the MLP down-projection forced onto it took 805 us
+// against 685 us).
+template <int RING>
+struct SmemLayout {
+    static constexpr int bar = RING;
+    static constexpr int sched = bar + 256;
+    static constexpr int stage = (sched + 4 * (2 * kMaxExperts + 2) + 127) & ~127;
+    static constexpr int bytes = stage + kStageBytesEpi;
+    static constexpr int alloc = bytes + 1024;  // slack for 1024-byte alignment
+};
+constexpr int kCarveout196 = 196 * 1024;
+using SmemCta = SmemLayout<kStages * kStageBytes>;
 
 template <int IT>
 struct InTraits;
@@ -358,7 +376,7 @@ __device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[16])
 }
 
 template <int IT, int OP, int ST, class EC, class ReleaseAcc>
-__device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, uint8_t* smem,
+__device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, float* stage,
                                               uint64_t* tfull, uint32_t tmem_base,
                                               volatile int* abort_flag, int warp, int lane,
                                               ReleaseAcc release_acc)
@@ -373,7 +391,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, 
     using Chunk = forge::Chunk<kChunkN>;
     const int mg = lane & 7;
     const int ns = lane >> 3;
-    float* stg = reinterpret_cast<float*>(smem + kSmemStageOffset) + ew * EC::stage_floats;
+    float* stg = stage + ew * EC::stage_floats;
     const int64_t M = p.M;
     const int64_t N = p.N;
     float gscale = 1.0f;
@@ -663,14 +681,14 @@ __global__ void __launch_bounds__(EpiFor<GROUPED>::threads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemBarOffset);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + SmemCta::bar);
     uint64_t* empty = full + kStages;
     uint64_t* tfull = empty + kStages;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int32_t* s_offs = reinterpret_cast<int32_t*>(smem + kSmemSchedOffset);
+    int32_t* s_offs = reinterpret_cast<int32_t*>(smem + SmemCta::sched);
     int32_t* s_order = s_offs + (kMaxExperts + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -874,7 +892,7 @@ __global__ void __launch_bounds__(EpiFor<GROUPED>::threads, 1)
         int npend = 0;  // stages issued but not yet announced, oldest first
         bool ok = true;
         for (int32_t it = 0; ok && it < sc.count; ++it) {
-                const int32_t t = sc.nth(it);
+            const int32_t t = sc.nth(it);
             const Tile tl = sc.get(t);
             for (int64_t k = tl.k_begin; k < tl.k_end; k += BK) {
                 // Announce every pending stage before blocking on a busy slot.
@@ -912,8 +930,9 @@ __global__ void __launch_bounds__(EpiFor<GROUPED>::threads, 1)
             for (; npend > 0; --npend) ptx::mbar_arrive(&full[(s - npend + kStages) % kStages]);
         }
     } else if (warp >= kEpiWarp0) {
-        epilogue_role<IT, OP, ST, EpiFor<GROUPED>>(p, sc, smem, tfull, tmem_base, abort_flag, warp, lane,
-                                  [&](uint32_t b) { ptx::mbar_arrive(&tempty[b]); });
+        epilogue_role<IT, OP, ST, EpiFor<GROUPED>>(
+            p, sc, reinterpret_cast<float*>(smem + SmemCta::stage), tfull, tmem_base, abort_flag,
+            warp, lane, [&](uint32_t b) { ptx::mbar_arrive(&tempty[b]); });
     }
 
     ptx::tc_fence_before();
@@ -950,11 +969,12 @@ __global__ void __launch_bounds__(EpiFor<GROUPED>::threads, 1)
 //   tfull[b]  (each CTA)  the pair's MMA commit, when accumulator b is complete
 //   tempty[b] (even CTA)  all 16 epilogue warps of the pair arrive (the odd
 //                         CTA's remotely) once accumulator b has been read
-constexpr int kPairStages = 6;
+constexpr int kPairStages = 5;
 constexpr int kPairStageA = 16384;  // this CTA's 128 rows of dY x BK
 constexpr int kPairStageB = 16384;  // this CTA's 128 columns of X x BK
 constexpr int kPairStageBytes = kPairStageA + kPairStageB;
-static_assert(kPairStages * kPairStageBytes <= kSmemBarOffset, "pair ring fits the stage area");
+using SmemPair = SmemLayout<kPairStages * kPairStageBytes>;
+static_assert(SmemPair::alloc + 1024 <= kCarveout196, "pair kernels keep a 60 KB L1");
 
 template <int IT, int OP, int ST, int NPAIR, bool GROUPED>
 __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUPED>::threads, 1)
@@ -980,14 +1000,14 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemBarOffset);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + SmemPair::bar);
     uint64_t* empty = full + kPairStages;
     uint64_t* tfull = empty + kPairStages;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int32_t* s_offs = reinterpret_cast<int32_t*>(smem + kSmemSchedOffset);
+    int32_t* s_offs = reinterpret_cast<int32_t*>(smem + SmemPair::sched);
     int32_t* s_order = s_offs + (kMaxExperts + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -1182,8 +1202,9 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
         }
     } else if (warp >= kEpiWarp0) {
         const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), lead_rank);
-        epilogue_role<IT, OP, ST, EpiFor<GROUPED>>(p, sc, smem, tfull, tmem_base, abort_flag, warp, lane,
-                                  [&](uint32_t b) {
+        epilogue_role<IT, OP, ST, EpiFor<GROUPED>>(
+            p, sc, reinterpret_cast<float*>(smem + SmemPair::stage), tfull, tmem_base, abort_flag,
+            warp, lane, [&](uint32_t b) {
                                       if (leader)
                                           ptx::mbar_arrive(&tempty[b]);
                                       else
