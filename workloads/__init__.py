@@ -172,5 +172,7 @@ ATTN_PROJ = [Workload(f"attn_proj K=16384 d_in=4096 d_out={m}", K=16384, N=4096,
                       adam=AdamHP(wd=0.1)) for m in ATTN_OUTS]
 MOE = Workload("moe E=8 tokens=16384 top2 d_in=14336 d_out=4096", K=32768, N=14336, M=4096,
                steps=6, experts=8)
+MOE_SMALL = Workload("moe_small E=2 tokens=4096 top2 d_in=14336 d_out=4096", K=8192, N=14336,
+                     M=4096, steps=1, experts=2)
 FP8 = Workload("fp8 K=32768 d_in=8192 d_out=8192", K=32768, N=8192, M=8192)
 FP8_SGD = SgdHP(lr=1e-2, momentum=0.9, wd=0.0)
