@@ -55,8 +55,8 @@ constexpr int kMaxExperts = 1024;
 
 // Epilogue geometry for EW epilogue warps.  Warp (q, grp) owns TMEM lane
 // quarter q and warp_cols accumulator columns, walked in chunks of
-// chunk_cols (n) x 32 (m); after a pass through shared memory a lane holds
-// four consecutive m for chunk_n consecutive n.  Sixteen warps with 8-column
+// chunk_cols (n) x 32 (m); after a transpose within each quad of lanes a lane
+// holds four consecutive m for chunk_n consecutive n.  Sixteen warps with 8-column
 // chunks keep more state loads in flight per SM (the epilogue-bound grouped
 // calls); eight warps with 16-column chunks leave more issue slots to the
 // producer and the MMA issuer (the MMA-bound dense calls).
@@ -70,37 +70,35 @@ struct Epi {
     static constexpr int chunk_cols = EW == 16 ? 8 : 16;
     static constexpr int chunk_n = chunk_cols / 4;
     static constexpr int chunks = warp_cols / chunk_cols;
-    static constexpr int stage_floats = chunk_cols * 32;  // per warp
 };
 template <bool GROUPED>
 using EpiFor = Epi<GROUPED ? 16 : 8>;
-constexpr int kStageBytesEpi = 16384;  // the epilogue warps' shared-memory stages
-static_assert(Epi<8>::warps * Epi<8>::stage_floats * 4 == kStageBytesEpi &&
-                  Epi<16>::warps * Epi<16>::stage_floats * 4 == kStageBytesEpi,
-              "one stage area for both geometries");
 
 // Shared memory of a kernel whose operand ring takes RING bytes: the ring,
-// the mbarriers, the grouped schedule (expert offsets and order) and the
-// epilogue stages.  Shared memory and L1 share 256 KB per SM, and the
-// carve-out is taken in steps (..., 164, 196, 228 KB).  The epilogue's
-// state loads land in L1 while in flight, so with the 228 KB step (a
-// 28 KB L1) an SM keeps too few of them outstanding: a decay-only stream
-// of W, m, v measured 4.5 TB/s there against 6.4 TB/s at the 196 KB step.
-// The CTA-pair kernels (every call with d_out > 128) take a five-stage ring
-// to stay within that step, the 1 KB the runtime keeps per block included.
-// The single-CTA kernel keeps four 48 KB stages and the 228 KB step: with
-// three its MMA starved (the MLP down-projection forced onto it took 805 us
-// against 685 us).
+// the mbarriers, then the grouped schedule (expert offsets and order), sized
+// per launch for the call's E experts.  Shared memory and L1 share 256 KB per
+// SM, and the carve-out is taken in steps (..., 164, 196, 228 KB).  The
+// epilogue's state loads occupy L1 while in flight: at the 228 KB step (a
+// 28 KB L1) a decay-only stream of W, m, v measured 4.5 TB/s, at the 196 KB
+// step (60 KB) 6.1 TB/s.  Both kernels' rings (six 32 KB stages per CTA of a
+// pair, four 48 KB stages for a single CTA) fit the 196 KB step with their
+// barriers and the table of up to kCarveoutExperts experts, the 1 KB the
+// runtime keeps per block included; calls with more experts take the next.
 template <int RING>
 struct SmemLayout {
     static constexpr int bar = RING;
     static constexpr int sched = bar + 256;
-    static constexpr int stage = (sched + 4 * (2 * kMaxExperts + 2) + 127) & ~127;
-    static constexpr int bytes = stage + kStageBytesEpi;
-    static constexpr int alloc = bytes + 1024;  // slack for 1024-byte alignment
+    // dynamic shared memory for a call over `experts` experts, with slack
+    // for the 1024-byte alignment of the ring
+    static constexpr int alloc(int experts)
+    {
+        return ((sched + 4 * (2 * experts + 2) + 127) & ~127) + 1024;
+    }
 };
 constexpr int kCarveout196 = 196 * 1024;
+constexpr int kCarveoutExperts = 128;
 using SmemCta = SmemLayout<kStages * kStageBytes>;
+static_assert(SmemCta::alloc(kCarveoutExperts) + 1024 <= kCarveout196, "196 KB step");
 
 template <int IT>
 struct InTraits;
@@ -319,8 +317,8 @@ struct StateIO<ST_BF16> {
     }
 };
 
-// One lane's share of a 16 (n) x 32 (m) accumulator chunk: four n rows of
-// four consecutive m each; element [jj * 4 + i] is (n = 4 ns + jj, m = 4 mg + i).
+// One lane's share of a (4 CN) (n) x 32 (m) accumulator chunk: CN n rows of
+// four consecutive m each; element [jj * 4 + i] is (n = CN ns + jj, m = 4 mg + i).
 template <int CN>
 struct Chunk {
     float g[4 * CN];
@@ -358,11 +356,11 @@ __device__ __forceinline__ void step4(const Params& p, const float* g, float* w,
 // Epilogue warps of one CTA (EC::warps of them, from warp kEpiWarp0).  Warp
 // (q, grp) owns TMEM lanes 32q..32q+31 (m) and columns EC::warp_cols grp ..
 // EC::warp_cols (grp + 1) - 1 (n) of the accumulator, walked in chunks.  Each
-// chunk goes TMEM -> registers (lane = m) -> a small smem stage -> registers
-// again with lane (mg, ns) holding m = 4 mg .. 4 mg + 3 for n = chunk_n ns ..
-// chunk_n ns + chunk_n - 1, so every global access is a 16-byte (fp32) or
-// 8-byte (bf16) vector and a warp instruction covers four 128-byte (or
-// 64-byte) row segments.  The state loads of chunk c+1 are in flight while
+// chunk goes TMEM -> registers (lane = m) -> a transpose within each quad of
+// lanes (shuffles, no shared memory) that leaves lane 4 mg + ns holding
+// m = 4 mg .. 4 mg + 3 for n = chunk_n ns .. chunk_n ns + chunk_n - 1, so every
+// global access is a 16-byte (fp32) or 8-byte (bf16) vector and a warp
+// instruction covers four 128-byte (or 64-byte) row segments.  The state loads of chunk c+1 are in flight while
 // chunk c is updated and stored.  `release_acc(b)` hands accumulator buffer b
 // back to the MMA issuer once it has been read.
 // One chunk of TMEM columns (the overload matches the chunk width).
@@ -375,8 +373,36 @@ __device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[16])
     ptx::tmem_ld_32x32b_x16(taddr, r);
 }
 
+// Lane 4 mg + i holds row m = 4 mg + i of a chunk: x[CN s + jj] is column
+// n = CN s + jj (s, i = 0..3).  Afterwards lane 4 mg + s holds column
+// n = CN s + jj of the four rows 4 mg + i in x[CN i + jj]: the 4 x 4
+// transpose of (lane within the quad) and s, for each jj, in two butterfly
+// exchanges, each swapping one bit of the lane index with the same bit of s.
+template <int CN>
+__device__ __forceinline__ void quad_transpose(float (&x)[4 * CN], int lane)
+{
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const bool up = (lane >> b) & 1;
+#pragma unroll
+        for (int jj = 0; jj < CN; ++jj)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                if (s & (1 << b)) continue;
+                const int lo = CN * s + jj;             // bit b of s clear
+                const int hi = CN * (s | (1 << b)) + jj;  // bit b of s set
+                // the element whose lane bit and s bit differ changes sides
+                const float recv = __shfl_xor_sync(0xffffffffu, up ? x[lo] : x[hi], 1 << b);
+                if (up)
+                    x[lo] = recv;
+                else
+                    x[hi] = recv;
+            }
+    }
+}
+
 template <int IT, int OP, int ST, class EC, class ReleaseAcc>
-__device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, float* stage,
+__device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc,
                                               uint64_t* tfull, uint32_t tmem_base,
                                               volatile int* abort_flag, int warp, int lane,
                                               ReleaseAcc release_acc)
@@ -389,9 +415,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, 
     constexpr int kChunkN = EC::chunk_n;
     constexpr int kChunks = EC::chunks;
     using Chunk = forge::Chunk<kChunkN>;
-    const int mg = lane & 7;
-    const int ns = lane >> 3;
-    float* stg = stage + ew * EC::stage_floats;
+    const int mg = lane >> 2;  // m group: lanes 4 mg .. 4 mg + 3 read TMEM rows 4 mg ..
+    const int ns = lane & 3;   // n group within the chunk after the quad transpose
     const int64_t M = p.M;
     const int64_t N = p.N;
     float gscale = 1.0f;
@@ -425,28 +450,23 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc, 
             if (lane == 0) release_acc(b);
         };
 
-        // The gradient of chunk c: TMEM -> registers -> stage -> this lane's
-        // 4 m x chunk_n n (zeros for a tile without tokens).
+        // The gradient of chunk c: TMEM -> registers (lane = m row) -> a 4 x 4
+        // transpose within each quad of lanes -> this lane's 4 m x chunk_n n
+        // (zeros for a tile without tokens).
         auto grad = [&](int c, Chunk& ch) {
             if (has_acc) {
                 uint32_t r[kChunkCols];
                 tmem_ld_chunk(tcol + kChunkCols * c, r);
                 ptx::tmem_ld_wait();
                 if (c == nchunks - 1) release();  // accumulator fully read
-                __syncwarp();  // previous chunk's stage reads are complete
+                float x[kChunkCols];
 #pragma unroll
-                for (int j = 0; j < kChunkCols; ++j)
-                    stg[j * 32 + lane] = __uint_as_float(r[j]) * gscale;
-                __syncwarp();
+                for (int j = 0; j < kChunkCols; ++j) x[j] = __uint_as_float(r[j]) * gscale;
+                quad_transpose<kChunkN>(x, lane);
 #pragma unroll
-                for (int jj = 0; jj < kChunkN; ++jj) {
-                    const float4 v =
-                        *reinterpret_cast<const float4*>(stg + (kChunkN * ns + jj) * 32 + 4 * mg);
-                    ch.g[jj * 4 + 0] = v.x;
-                    ch.g[jj * 4 + 1] = v.y;
-                    ch.g[jj * 4 + 2] = v.z;
-                    ch.g[jj * 4 + 3] = v.w;
-                }
+                for (int jj = 0; jj < kChunkN; ++jj)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) ch.g[jj * 4 + i] = x[kChunkN * i + jj];
             } else {
 #pragma unroll
                 for (int j = 0; j < 4 * kChunkN; ++j) ch.g[j] = 0.0f;
@@ -689,7 +709,7 @@ __global__ void __launch_bounds__(EpiFor<GROUPED>::threads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int32_t* s_offs = reinterpret_cast<int32_t*>(smem + SmemCta::sched);
-    int32_t* s_order = s_offs + (kMaxExperts + 1);
+    int32_t* s_order = s_offs + (p.E + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -931,8 +951,8 @@ __global__ void __launch_bounds__(EpiFor<GROUPED>::threads, 1)
         }
     } else if (warp >= kEpiWarp0) {
         epilogue_role<IT, OP, ST, EpiFor<GROUPED>>(
-            p, sc, reinterpret_cast<float*>(smem + SmemCta::stage), tfull, tmem_base, abort_flag,
-            warp, lane, [&](uint32_t b) { ptx::mbar_arrive(&tempty[b]); });
+            p, sc, tfull, tmem_base, abort_flag, warp, lane,
+            [&](uint32_t b) { ptx::mbar_arrive(&tempty[b]); });
     }
 
     ptx::tc_fence_before();
@@ -969,12 +989,12 @@ __global__ void __launch_bounds__(EpiFor<GROUPED>::threads, 1)
 //   tfull[b]  (each CTA)  the pair's MMA commit, when accumulator b is complete
 //   tempty[b] (even CTA)  all 16 epilogue warps of the pair arrive (the odd
 //                         CTA's remotely) once accumulator b has been read
-constexpr int kPairStages = 5;
+constexpr int kPairStages = 6;
 constexpr int kPairStageA = 16384;  // this CTA's 128 rows of dY x BK
 constexpr int kPairStageB = 16384;  // this CTA's 128 columns of X x BK
 constexpr int kPairStageBytes = kPairStageA + kPairStageB;
 using SmemPair = SmemLayout<kPairStages * kPairStageBytes>;
-static_assert(SmemPair::alloc + 1024 <= kCarveout196, "pair kernels keep a 60 KB L1");
+static_assert(SmemPair::alloc(kCarveoutExperts) + 1024 <= kCarveout196, "196 KB step");
 
 template <int IT, int OP, int ST, int NPAIR, bool GROUPED>
 __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUPED>::threads, 1)
@@ -1008,7 +1028,7 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int32_t* s_offs = reinterpret_cast<int32_t*>(smem + SmemPair::sched);
-    int32_t* s_order = s_offs + (kMaxExperts + 1);
+    int32_t* s_order = s_offs + (p.E + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1203,8 +1223,7 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
     } else if (warp >= kEpiWarp0) {
         const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), lead_rank);
         epilogue_role<IT, OP, ST, EpiFor<GROUPED>>(
-            p, sc, reinterpret_cast<float*>(smem + SmemPair::stage), tfull, tmem_base, abort_flag,
-            warp, lane, [&](uint32_t b) {
+            p, sc, tfull, tmem_base, abort_flag, warp, lane, [&](uint32_t b) {
                                       if (leader)
                                           ptx::mbar_arrive(&tempty[b]);
                                       else

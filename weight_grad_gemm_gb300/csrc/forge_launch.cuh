@@ -40,12 +40,12 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
         int& mc = max_clusters[dev & 63];                                                      \
         if (__atomic_load_n(&mc, __ATOMIC_ACQUIRE) == 0) {                                     \
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
-                                     SmemPair::alloc);                                         \
+                                     SmemPair::alloc(kMaxExperts));                            \
             if (e != cudaSuccess) return e;                                                    \
             cudaLaunchConfig_t cfg = {};                                                       \
             cfg.gridDim = dim3(2 * NPAIR, 1, 1);                                               \
             cfg.blockDim = dim3(EpiFor<GROUPED>::threads, 1, 1);                               \
-            cfg.dynamicSmemBytes = SmemPair::alloc;                                            \
+            cfg.dynamicSmemBytes = SmemPair::alloc(kMaxExperts);                               \
             int n = 0;                                                                         \
             e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);                                \
             if (e != cudaSuccess) return e;                                                    \
@@ -53,7 +53,7 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
             __atomic_store_n(&mc, n, __ATOMIC_RELEASE);                                        \
         }                                                                                      \
         const int64_t nc = total_tiles < mc ? total_tiles : mc;                                \
-        kern<<<static_cast<int>(2 * NPAIR * nc), EpiFor<GROUPED>::threads, SmemPair::alloc,    \
+        kern<<<static_cast<int>(2 * NPAIR * nc), EpiFor<GROUPED>::threads, SmemPair::alloc(p.E), \
                stream>>>(                                                                      \
             tmA, tmB, tmA1, tmB1, p);                                                          \
         return cudaGetLastError();                                                             \
@@ -80,11 +80,12 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
         const unsigned long long bit = 1ull << (dev & 63);                                     \
         if (!(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {                          \
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
-                                     SmemCta::alloc);                                          \
+                                     SmemCta::alloc(kMaxExperts));                             \
             if (e != cudaSuccess) return e;                                                    \
             __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);                              \
         }                                                                                      \
-        kern<<<grid, EpiFor<GROUPED>::threads, SmemCta::alloc, stream>>>(tmA, tmB, tmA1, tmB1, \
+        kern<<<grid, EpiFor<GROUPED>::threads, SmemCta::alloc(p.E), stream>>>(                 \
+            tmA, tmB, tmA1, tmB1,                                                              \
                                                                      p);                       \
         return cudaGetLastError();                                                             \
     }                                                                                          \
