@@ -222,7 +222,9 @@ bool stage_misaligned()
 // The four operand maps of one call: dY and X with whole k-block boxes, and
 // (grouped calls) the same tensors with one-row boxes for gathered blocks.
 struct Maps {
-    CUtensorMap a, b, a1, b1;
+    CUtensorMap a, b;    // boxes of one k-block (BK token rows)
+    CUtensorMap a1, b1;  // grouped: one-row boxes (four-row gathers)
+    CUtensorMap ak, bk;  // grouped: boxes of one MMA k-step (an expert's last k-block)
 };
 
 template <int IT, bool MAN>
@@ -247,7 +249,8 @@ template <int IT, int NP>
 cudaError_t dispatch_pair(int op, int st, bool grouped, const Maps& m, const Params& p,
                           int64_t grid, cudaStream_t s)
 {
-#define FORGE_L(OPV, STV, G) launch_wgrad_pair<IT, OPV, STV, NP, G>(m.a, m.b, m.a1, m.b1, p, grid, s)
+#define FORGE_L(OPV, STV, G) \
+    launch_wgrad_pair<IT, OPV, STV, NP, G>(m.a, m.b, m.a1, m.b1, m.ak, m.bk, p, grid, s)
     if constexpr (NP == 1) {
         if (grouped)
             return st == ST_F32 ? FORGE_L(OP_ADAMW, ST_F32, true) : FORGE_L(OP_ADAMW, ST_BF16, true);
@@ -410,6 +413,11 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
             st = encode_operand(&maps.a1, opA, in_dtype, p.M, rows, ldA, 0);
         if (st == FORGE_OK && grouped && !p.manual_b)
             st = encode_operand(&maps.b1, opB, in_dtype, p.N, rows, ldB, 0);
+        // one MMA k-step (16 bf16 or 32 e4m3 rows) = a quarter of a k-block
+        if (st == FORGE_OK && grouped && !p.manual_a)
+            st = encode_operand(&maps.ak, opA, in_dtype, p.M, rows, ldA, 4);
+        if (st == FORGE_OK && grouped && !p.manual_b)
+            st = encode_operand(&maps.bk, opB, in_dtype, p.N, rows, ldB, 4);
         if (st != FORGE_OK) {
             if (scratch) scratch_free(scratch, stream);
             return st;

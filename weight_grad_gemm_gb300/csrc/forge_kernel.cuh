@@ -1002,10 +1002,14 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
                             const __grid_constant__ CUtensorMap tmB,   // X, boxes of BK / NPAIR rows
                             const __grid_constant__ CUtensorMap tmA1,  // dY, one-row boxes (grouped)
                             const __grid_constant__ CUtensorMap tmB1,  // X, one-row boxes (grouped)
+                            const __grid_constant__ CUtensorMap tmAk,  // dY, one-k-step boxes (grouped)
+                            const __grid_constant__ CUtensorMap tmBk,  // X, one-k-step boxes (grouped)
                             const Params p)
 {
     static_assert(NPAIR == 1 || NPAIR == 2, "one or two pairs per cluster");
     static_assert(!GROUPED || NPAIR == 1, "grouped calls use single pairs");
+    static_assert(InTraits<IT>::BK == 4 * InTraits<IT>::umma_k,
+                  "the one-k-step maps hold a quarter of a k-block");
     using TR = InTraits<IT>;
     constexpr int BK = TR::BK;
     constexpr int kBoxBytes = TR::box_mn * TR::esize * BK;
@@ -1111,18 +1115,50 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
                     const int32_t ky = static_cast<int32_t>(k);
                     const int32_t nb = tl.n0 + static_cast<int32_t>(rank) * (BN / 2);
                     if (GROUPED && tl.k_end - k < BK) {
-                        const int32_t kend = static_cast<int32_t>(tl.k_end);
+                        // The expert's last k-block carries valid < BK token
+                        // rows.  Its whole MMA k-steps come as k-step-high
+                        // boxes; the incomplete one four rows at a time, rows
+                        // past the expert's end read as zeros; the k-steps
+                        // after it as boxes starting past the tensor's last
+                        // row, which TMA fills with zeros.  Every row of
+                        // another expert stays out of the product.
+                        const int32_t valid = static_cast<int32_t>(tl.k_end - k);
+                        const int32_t whole = valid / TR::umma_k;
+                        const int32_t steps = (valid + TR::umma_k - 1) / TR::umma_k;
                         const int32_t oob = static_cast<int32_t>(p.T_max);
-                        gather_block<BK, kABoxes, TR::box_mn, kBoxBytes>(
-                            tl.m0, ky, kend, oob, [&](int off, int32_t x, const int32_t* y) {
-                                ptx::tma_gather4_2d_pair(sa + off, &tmA1, bar, x, y[0], y[1], y[2],
-                                                         y[3]);
-                            });
-                        gather_block<BK, kBBoxes, TR::box_mn, kBoxBytes>(
-                            nb, ky, kend, oob, [&](int off, int32_t x, const int32_t* y) {
-                                ptx::tma_gather4_2d_pair(sb + off, &tmB1, bar, x, y[0], y[1], y[2],
-                                                         y[3]);
-                            });
+#pragma unroll 1
+                        for (int32_t j = 0; j < kKSteps; ++j) {
+                            if (j == whole && whole < steps) continue;  // gathered below
+                            const int off = j * TR::umma_k * 128;
+                            const int32_t y = j < whole ? ky + j * TR::umma_k : oob;
+#pragma unroll
+                            for (int i = 0; i < kABoxes; ++i)
+                                ptx::tma_load_2d_pair(sa + i * kBoxBytes + off, &tmAk, bar,
+                                                      tl.m0 + i * TR::box_mn, y);
+#pragma unroll
+                            for (int i = 0; i < kBBoxes; ++i)
+                                ptx::tma_load_2d_pair(sb + i * kBoxBytes + off, &tmBk, bar,
+                                                      nb + i * TR::box_mn, y);
+                        }
+                        if (whole < steps) {
+                            const int32_t kend = static_cast<int32_t>(tl.k_end);
+#pragma unroll 1
+                            for (int32_t r = whole * TR::umma_k; r < steps * TR::umma_k; r += 4) {
+                                int32_t y[4];
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) y[j] = ky + r + j < kend ? ky + r + j : oob;
+#pragma unroll
+                                for (int i = 0; i < kABoxes; ++i)
+                                    ptx::tma_gather4_2d_pair(sa + i * kBoxBytes + r * 128, &tmA1, bar,
+                                                             tl.m0 + i * TR::box_mn, y[0], y[1], y[2],
+                                                             y[3]);
+#pragma unroll
+                                for (int i = 0; i < kBBoxes; ++i)
+                                    ptx::tma_gather4_2d_pair(sb + i * kBoxBytes + r * 128, &tmB1, bar,
+                                                             nb + i * TR::box_mn, y[0], y[1], y[2],
+                                                             y[3]);
+                            }
+                        }
                     } else {
 #pragma unroll
                         for (int i = 0; i < kABoxes; ++i)

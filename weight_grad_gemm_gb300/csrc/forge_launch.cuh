@@ -20,7 +20,8 @@ cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB, const C
 // in one GPC), never more than `total_tiles` clusters.
 template <int IT, int OP, int ST, int NPAIR, bool GROUPED>
 cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
-                              const CUtensorMap& tmA1, const CUtensorMap& tmB1, const Params& p,
+                              const CUtensorMap& tmA1, const CUtensorMap& tmB1,
+                              const CUtensorMap& tmAk, const CUtensorMap& tmBk, const Params& p,
                               int64_t total_tiles, cudaStream_t stream);
 
 }  // namespace forge
@@ -30,6 +31,7 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
     template <int IT, int OP, int ST, int NPAIR, bool GROUPED>                                 \
     cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,              \
                                   const CUtensorMap& tmA1, const CUtensorMap& tmB1,            \
+                                  const CUtensorMap& tmAk, const CUtensorMap& tmBk,            \
                                   const Params& p, int64_t total_tiles, cudaStream_t stream)   \
     {                                                                                          \
         static int max_clusters[64] = {0};                                                     \
@@ -55,7 +57,7 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
         const int64_t nc = total_tiles < mc ? total_tiles : mc;                                \
         kern<<<static_cast<int>(2 * NPAIR * nc), EpiFor<GROUPED>::threads, SmemPair::alloc(p.E), \
                stream>>>(                                                                      \
-            tmA, tmB, tmA1, tmB1, p);                                                          \
+            tmA, tmB, tmA1, tmB1, tmAk, tmBk, p);                                              \
         return cudaGetLastError();                                                             \
     }                                                                                          \
     }
@@ -63,6 +65,7 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
 #define FORGE_INSTANTIATE_PAIR(IT, OP, ST, NPAIR, G)                                           \
     template cudaError_t forge::launch_wgrad_pair<IT, OP, ST, NPAIR, G>(                       \
         const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,        \
+        const CUtensorMap&, const CUtensorMap&,                                                \
         const forge::Params&, int64_t, cudaStream_t);
 
 #define FORGE_DEFINE_LAUNCH()                                                                  \
