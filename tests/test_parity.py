@@ -283,6 +283,18 @@ def test_grouped_e4m3(cuda_device, grouped_form):
     check_grouped(got, X, D, off, W, m, v, 2, sc, False)
 
 
+@pytest.mark.parametrize("kind", ["bf16", "e4m3"])
+def test_grouped_tails_on_k_step_boundaries(cuda_device, grouped_form, kind):
+    """Experts whose last k-block ends on an MMA k-step (16 bf16 or 32 e4m3
+    token rows) or one row past or short of one: whole k-steps, k-steps with
+    rows of the next expert behind them, and blocks shorter than a k-step."""
+    counts = [96, 16, 48, 80, 113, 1] if kind == "bf16" else [160, 32, 96, 64, 161, 31]
+    N, M = 264, 392
+    X, D, off, W, m, v, sc = grouped_case(counts, N, M, 17, kind=kind)
+    got = run_grouped(cuda_device, X, D, off, W, m, v, step=2, scales=sc)
+    check_grouped(got, X, D, off, W, m, v, 2, sc, False)
+
+
 def test_grouped_all_experts_empty(cuda_device, grouped_form):
     counts = [0, 0, 0]
     N, M = 256, 128
