@@ -9,8 +9,10 @@ The default workload is the Llama-style MLP down-projection (K = 8192
 tokens, d_in = 14336, d_out = 4096, bf16 X / dY, fp32 W / m / v, AdamW
 step t = 4 onward).  ``value`` is TFLOP/s = 2 M N K / (device time per step),
 with inputs resident in HBM; ``e2e`` is the same metric through the C ABI
-with pinned host buffers (host->device copies of X and dY and the
-device->host copy of the updated W inside the timed region).
+with pinned host buffers: every step copies its X and dY in and its updated
+W out inside the timed region, the upload of the next step and the read-back
+of the previous one overlapping the current step (``sequential_value``: the
+same with each step alone).
 
 Multi-GPU: the path is replicated (each rank runs its own full workload, no
 collective on the data path); value sums over ranks and the time is the max
@@ -676,6 +678,82 @@ def run_ncu(args):
     return 0
 
 
+# ---------------------------------------------------------------- end to end
+
+def e2e_sequential(job, ins_h, res_h, dev, stream, flush, steps):
+    """Milliseconds per step with each step alone: copy in, step, copy out."""
+    ins_d = [torch.empty_like(h, device=dev) for h in ins_h]
+    times = []
+    for i in range(steps + 2):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            for d, h in zip(ins_d, ins_h):
+                d.copy_(h, non_blocking=True)
+            job.step_with(ins_d, stream=stream)
+            res_h.copy_(job.result(), non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 2:
+            times.append(a.elapsed_time(b))
+    return float(np.mean(times)) if times else float("nan")
+
+
+def e2e_pipelined(job, ins_h, res_h, dev, stream, steps):
+    """Milliseconds per step over `steps` back-to-back steps, each with its
+    own host->device copy of the inputs and device->host copy of the updated
+    parameters.  The upload of step i+1 (double-buffered inputs, its own
+    stream) overlaps step i; step i's parameters are snapshotted on the
+    device right after it and read back on a third stream while step i+1
+    runs (the next step updates W in place)."""
+    res = job.result()
+    bufs = [[torch.empty_like(h, device=dev) for h in ins_h] for _ in range(2)]
+    snap = torch.empty_like(res)
+    up = torch.cuda.Stream(dev)
+    down = torch.cuda.Stream(dev)
+
+    def run(n):
+        ready = [torch.cuda.Event() for _ in range(2)]
+        used = [torch.cuda.Event() for _ in range(2)]
+        taken, read = torch.cuda.Event(), torch.cuda.Event()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        up.wait_event(a)
+        down.wait_event(a)
+        for i in range(n):
+            k = i % 2
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(used[k])  # step i-2 is done with this buffer
+                for d, h in zip(bufs[k], ins_h):
+                    d.copy_(h, non_blocking=True)
+                ready[k].record(up)
+            stream.wait_event(ready[k])
+            job.step_with(bufs[k], stream=stream)
+            used[k].record(stream)
+            if i >= 1:
+                stream.wait_event(read)  # the previous read-back is done with the snapshot
+            with torch.cuda.stream(stream):
+                snap.copy_(res, non_blocking=True)
+            taken.record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(taken)
+                res_h.copy_(snap, non_blocking=True)
+                read.record(down)
+        stream.wait_event(read)
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / max(n, 1)
+
+    run(2)  # warm-up
+    return run(steps)
+
+
 # ---------------------------------------------------------------- our arm
 
 def main():
@@ -685,7 +763,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference", "unfused"])
     ap.add_argument("--workload", default="mlp_down", choices=sorted(WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--state", default="f32", choices=["f32", "bf16"],
                     help="optimizer state type (default fp32, the headline workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -758,30 +836,14 @@ def main():
     ms = total_ms / args.steps
     value = whole_job_rate(job.flops, world, ms)
 
-    # end to end through the C ABI with pinned host buffers: this step's
-    # inputs are copied in and the updated parameters copied out, every step
-    ins = job.inputs()
-    ins_h = [t.cpu().pin_memory() for t in ins]
-    ins_d = [torch.empty_like(t) for t in ins]
-    res = job.result()
-    res_h = torch.empty(res.shape, dtype=res.dtype).pin_memory()
-    e2e_times = []
-    for i in range(args.e2e_steps + 2):
-        flush.zero_()
-        torch.cuda.synchronize(dev)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for d, h in zip(ins_d, ins_h):
-            d.copy_(h, non_blocking=True)
-        job.step_with(ins_d, stream=stream)
-        with torch.no_grad():
-            res_h.copy_(job.result(), non_blocking=True)
-        b.record(stream)
-        b.synchronize()
-        if i >= 2:
-            e2e_times.append(a.elapsed_time(b))
-    e2e_ms = max_over_ranks(float(np.mean(e2e_times)) if e2e_times else float("nan"), world, dev)
+    # end to end through the C ABI with pinned host buffers: every step's
+    # inputs are copied in and its updated parameters copied out
+    ins_h = [t.cpu().pin_memory() for t in job.inputs()]
+    res_h = torch.empty(job.result().shape, dtype=job.result().dtype).pin_memory()
+    e2e_seq_ms = max_over_ranks(e2e_sequential(job, ins_h, res_h, dev, stream, flush,
+                                               args.e2e_steps), world, dev)
+    e2e_ms = max_over_ranks(e2e_pipelined(job, ins_h, res_h, dev, stream, args.e2e_steps),
+                            world, dev)
     h2d = sum(h.numel() * h.element_size() for h in ins_h)
     d2h = res_h.numel() * res_h.element_size()
 
@@ -820,7 +882,9 @@ def main():
                      # the same against the power-capped (seconds-long) cuBLAS rate
                      "frac_sustained": kernel_tf / (peak_tf * sustained_ratio)},
         "e2e": {"value": whole_job_rate(job.flops, world, e2e_ms), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms, "pipelined": True,
+                "sequential_value": whole_job_rate(job.flops, world, e2e_seq_ms)},
         "gpu_launches": args.steps * getattr(job, "launches", 1) if args.impl == "ours" else 0,
         "clocks": clk,
         "wall_s_timed_region": wall,
