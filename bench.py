@@ -232,7 +232,13 @@ class Backward(Dense):
 class AttnSet:
     """The four attention projections of one layer (d_in 4096, d_out 4096,
     1024, 1024, 4100; K = 16384) as four fused calls per step; d_out = 4100
-    has 8200-byte dY rows, which the library stages into 16-byte rows."""
+    has 8200-byte dY rows, which the library stages into 16-byte rows.
+
+    The calls are independent (their own dY, W, m, v; X read by all), so each
+    goes on its own stream, forked from and joined back to the caller's: a
+    call's persistent grid covers only its own tiles (64 CTA pairs of 76 for
+    d_out = 1024), and the SMs it leaves idle, or frees in its last wave, run
+    the next call's tiles."""
 
     peak_key = "bf16"
     opt = "AdamW"
@@ -248,17 +254,32 @@ class AttnSet:
         self.params = sum(p.params for p in self.parts)
         self.bytes = sum(p.bytes for p in self.parts)
         self.launches = sum(p.launches for p in self.parts)
+        self.dev = dev
+        self.side = [torch.cuda.Stream(dev) for _ in self.parts]
+
+    def _fan_out(self, stream, calls):
+        main = stream if stream is not None else torch.cuda.current_stream(self.dev)
+        go = torch.cuda.Event()
+        go.record(main)
+        done = []
+        for s, call in zip(self.side, calls):
+            s.wait_event(go)
+            call(s)
+            e = torch.cuda.Event()
+            e.record(s)
+            done.append(e)
+        for e in done:
+            main.wait_event(e)
 
     def step(self, stream=None):
-        for p in self.parts:
-            p.step(stream=stream)
+        self._fan_out(stream, [lambda s, p=p: p.step(stream=s) for p in self.parts])
 
     def inputs(self):
         return [self.parts[0].X] + [p.D for p in self.parts]
 
     def step_with(self, ins, stream=None):
-        for i, p in enumerate(self.parts):
-            p.step(ins[0], ins[1 + i], stream=stream)
+        self._fan_out(stream, [lambda s, i=i, p=p: p.step(ins[0], ins[1 + i], stream=s)
+                               for i, p in enumerate(self.parts)])
 
     def result(self):
         return self.parts[0].W
