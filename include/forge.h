@@ -162,6 +162,37 @@ FORGE_API forge_status forge_wgrad_adamw_noalloc(const void* X, const void* dY, 
                                                  forge_stream_t stream);
 
 /*
+ * Several AdamW weight-gradient steps that share X, in one launch: for each
+ * problem j < P, dW_j = X^T dY_j and one AdamW step on W_j, m_j, v_j, exactly
+ * as forge_wgrad_adamw(X, dY[j], W[j], m[j], v[j], M[j], N, K, ...) would
+ * compute it (bitwise wherever that call runs on CTA pairs, M[j] > 128: the
+ * same 256 x 256 tiles in the same K order).  For layers whose
+ * projections read the same activations (an attention block's projections):
+ * the problems' tiles form one list walked by one grid, so SMs that a small
+ * problem alone would leave idle run the others' tiles.  The operation of
+ * each problem is the one forge_wgrad_adamw states; the pages know no
+ * batched form of it.
+ *   X            device bf16 [K, N], shared by all problems.
+ *   P            1 <= P <= 8 problems.
+ *   dY, M, W, m, v   host arrays of P entries: device bf16 dY[j] [K, M[j]],
+ *                device fp32 W[j] and state_dtype m[j], v[j] [N, M[j]]
+ *                (pointers the caller owns; the arrays are read during the
+ *                call only).  Problems must not share W, m or v.
+ *   in_dtype     FORGE_BF16 only (else FORGE_ERR_UNSUPPORTED_DTYPE).
+ *   state_dtype, lr, beta1, beta2, eps, wd, step: as forge_wgrad_adamw, the
+ *                same for every problem.
+ * Checks as forge_wgrad_adamw, per problem, before any launch; an operand
+ * whose rows TMA cannot address is staged into the library's memory pool
+ * (one allocation per call), and a failed allocation returns FORGE_ERR_CUDA.
+ */
+FORGE_API forge_status forge_wgrad_adamw_multi(const void* X, int64_t N, int64_t K, int32_t P,
+                                               const void* const* dY, const int64_t* M,
+                                               float* const* W, void* const* m, void* const* v,
+                                               forge_dtype in_dtype, forge_dtype state_dtype,
+                                               float lr, float beta1, float beta2, float eps,
+                                               float wd, int64_t step, forge_stream_t stream);
+
+/*
  * Per-tensor e4m3 quantisation with an amax scale, the step in front of an
  * fp8 call (the fp8 rows of "Math verified, not asserted", P6; the recipe
  * s = amax / 448 of the fp8 workload):

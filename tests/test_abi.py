@@ -113,6 +113,33 @@ def test_grouped_rejects_invalid_arguments(L):
     assert g(step=0) == fg.FORGE_ERR_INVALID_ARG
 
 
+def multi(L, P=3, M=(64, 32, 72), dY=FAKE, W=FAKE, null_entry=None, N=64, K=64,
+          it=fg.FORGE_BF16, st=fg.FORGE_F32, hp=HP, step=1, arrays=True):
+    arr = ctypes.c_void_p * 8
+    d = arr(*([dY] * 8))
+    w, m, v = arr(*([W] * 8)), arr(*([FAKE] * 8)), arr(*([FAKE] * 8))
+    if null_entry is not None:
+        {"dY": d, "W": w, "m": m, "v": v}[null_entry][1] = None
+    ms = (ctypes.c_int64 * 8)(*(list(M) + [64] * (8 - len(M))))
+    return L.forge_wgrad_adamw_multi(FAKE, N, K, P, d if arrays else None, ms, w, m, v, it, st,
+                                     *hp, step, None)
+
+
+def test_multi_rejects_invalid_arguments(L):
+    assert multi(L, P=0) == fg.FORGE_ERR_INVALID_ARG
+    assert multi(L, P=9) == fg.FORGE_ERR_INVALID_ARG
+    assert multi(L, arrays=False) == fg.FORGE_ERR_INVALID_ARG
+    for which in ("dY", "W", "m", "v"):
+        assert multi(L, null_entry=which) == fg.FORGE_ERR_INVALID_ARG
+    assert multi(L, M=(64, 0, 72)) == fg.FORGE_ERR_INVALID_ARG
+    assert multi(L, N=0) == fg.FORGE_ERR_INVALID_ARG
+    assert multi(L, K=-1) == fg.FORGE_ERR_INVALID_ARG
+    assert multi(L, step=0) == fg.FORGE_ERR_INVALID_ARG
+    assert multi(L, hp=(1e-3, 0.9, 1.0, 1e-8, 0.01)) == fg.FORGE_ERR_INVALID_ARG
+    assert multi(L, it=fg.FORGE_E4M3) == fg.FORGE_ERR_UNSUPPORTED_DTYPE
+    assert multi(L, st=fg.FORGE_E4M3) == fg.FORGE_ERR_UNSUPPORTED_DTYPE
+
+
 def test_quantize_rejects_invalid_arguments(L):
     def q(x=FAKE, dt=fg.FORGE_F32, n=64, codes=FAKE, scale=FAKE):
         return L.forge_quantize_e4m3(x, dt, n, codes, scale, None)
@@ -157,6 +184,7 @@ def test_valid_call_without_gpu_fails_closed(L):
         pytest.skip("a GPU is present; the fake pointers must not reach a kernel")
     assert adamw(L) == fg.FORGE_ERR_UNSUPPORTED_DEVICE
     assert adamw(L, fn="forge_wgrad_adamw_noalloc") == fg.FORGE_ERR_UNSUPPORTED_DEVICE
+    assert multi(L) == fg.FORGE_ERR_UNSUPPORTED_DEVICE
     assert L.forge_dgrad(FAKE, FAKE, FAKE, 64, 64, 64, fg.FORGE_BF16, None) == \
         fg.FORGE_ERR_UNSUPPORTED_DEVICE
     assert fg.forge_get_device_status() == fg.FORGE_ERR_UNSUPPORTED_DEVICE

@@ -33,7 +33,8 @@ FORGE_BF16 = 0
 FORGE_E4M3 = 1
 FORGE_F32 = 2
 
-EXPORTS = ("forge_wgrad_adamw", "forge_wgrad_adamw_noalloc", "forge_wgrad_sgdm", "forge_wgrad_only",
+EXPORTS = ("forge_wgrad_adamw", "forge_wgrad_adamw_noalloc", "forge_wgrad_adamw_multi",
+           "forge_wgrad_sgdm", "forge_wgrad_only",
            "forge_quantize_e4m3", "forge_dgrad", "forge_backward_adamw",
            "forge_grouped_wgrad_adamw", "forge_status_string", "forge_get_device_status",
            "forge_selftest_wait_timeout", "forge_version")
@@ -60,6 +61,8 @@ def lib() -> ctypes.CDLL:
                          ctypes.c_int)
     L.forge_wgrad_adamw.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, F, F, F, F, F, I64, P, P]
     L.forge_wgrad_adamw_noalloc.argtypes = L.forge_wgrad_adamw.argtypes
+    L.forge_wgrad_adamw_multi.argtypes = [P, I64, I64, I32, P, P, P, P, P, I, I, F, F, F, F, F,
+                                          I64, P]
     L.forge_quantize_e4m3.argtypes = [P, I, I64, P, P, P]
     L.forge_dgrad.argtypes = [P, P, P, I64, I64, I64, I, P]
     L.forge_backward_adamw.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I, I, F, F, F, F, F,
@@ -68,7 +71,8 @@ def lib() -> ctypes.CDLL:
     L.forge_wgrad_only.argtypes = [P, P, P, I64, I64, I64, I, P, P]
     L.forge_grouped_wgrad_adamw.argtypes = [P, P, P, P, P, P, I32, I64, I64, I64, I, I, F, F, F,
                                             F, F, I64, P, P]
-    for f in ("forge_wgrad_adamw", "forge_wgrad_adamw_noalloc", "forge_wgrad_sgdm",
+    for f in ("forge_wgrad_adamw", "forge_wgrad_adamw_noalloc", "forge_wgrad_adamw_multi",
+              "forge_wgrad_sgdm",
               "forge_wgrad_only", "forge_quantize_e4m3", "forge_dgrad", "forge_backward_adamw",
               "forge_grouped_wgrad_adamw", "forge_get_device_status",
               "forge_selftest_wait_timeout"):
@@ -160,6 +164,35 @@ def forge_wgrad_adamw_noalloc(X, dY, W, m, v, *, lr, beta1, beta2, eps, wd, step
     per-device buffer instead of allocating (see include/forge.h)."""
     _adamw_call("forge_wgrad_adamw_noalloc", X, dY, W, m, v, lr, beta1, beta2, eps, wd, step,
                 scales, stream)
+
+
+def forge_wgrad_adamw_multi(X, dYs, Ws, ms, vs, *, lr, beta1, beta2, eps, wd, step,
+                            stream=None):
+    """One launch of forge_wgrad_adamw for each (dY, W, m, v) of the lists, all
+    with the same X (see include/forge.h)."""
+    n = len(dYs)
+    if not (len(Ws) == len(ms) == len(vs) == n):
+        raise ValueError("dYs, Ws, ms, vs must have one entry per problem")
+    sizes = [_sizes(X, d) for d in dYs]
+    N, K = X.shape[1], X.shape[0]
+    for (M, _, _), W, m, v in zip(sizes, Ws, ms, vs):
+        for t in (W, m, v):
+            if tuple(t.shape) != (N, M):
+                raise ValueError(f"W/m/v must be [N={N}, M={M}], got {tuple(t.shape)}")
+        if m.dtype != v.dtype or m.dtype != ms[0].dtype:
+            raise TypeError("every m and v must share one dtype")
+        if X.dtype != dYs[0].dtype:
+            raise TypeError("X and every dY must share one dtype")
+    arr = ctypes.c_void_p * max(n, 1)
+    dptr = arr(*[_ptr(d).value for d in dYs])
+    wptr = arr(*[_ptr(t).value for t in Ws])
+    mptr = arr(*[_ptr(t).value for t in ms])
+    vptr = arr(*[_ptr(t).value for t in vs])
+    mlen = (ctypes.c_int64 * max(n, 1))(*[M for M, _, _ in sizes])
+    s = lib().forge_wgrad_adamw_multi(_ptr(X), N, K, n, dptr, mlen, wptr, mptr, vptr,
+                                      _dtype_code(X), _dtype_code(ms[0]), lr, beta1, beta2, eps,
+                                      wd, int(step), _stream(stream, Ws[0]))
+    _check(s, "forge_wgrad_adamw_multi")
 
 
 def forge_wgrad_sgdm(X, dY, W, mom, *, lr, momentum, wd, scales=None, stream=None):

@@ -221,6 +221,9 @@ bool stage_misaligned()
 
 // The four operand maps of one call: dY and X with whole k-block boxes, and
 // (grouped calls) the same tensors with one-row boxes for gathered blocks.
+// The problem table's maps of a call that is not a multi-problem call.
+const MultiMaps kNoProblemMaps = {};
+
 struct Maps {
     CUtensorMap a, b;    // boxes of one k-block (BK token rows)
     CUtensorMap a1, b1;  // grouped: one-row boxes (four-row gathers)
@@ -249,8 +252,9 @@ template <int IT, int NP>
 cudaError_t dispatch_pair(int op, int st, bool grouped, const Maps& m, const Params& p,
                           int64_t grid, cudaStream_t s)
 {
-#define FORGE_L(OPV, STV, G) \
-    launch_wgrad_pair<IT, OPV, STV, NP, G>(m.a, m.b, m.a1, m.b1, m.ak, m.bk, p, grid, s)
+#define FORGE_L(OPV, STV, G)                                                       \
+    launch_wgrad_pair<IT, OPV, STV, NP, G, false>(m.a, m.b, m.a1, m.b1, m.ak, m.bk, \
+                                                  kNoProblemMaps, p, grid, s)
     if constexpr (NP == 1) {
         if (grouped)
             return st == ST_F32 ? FORGE_L(OP_ADAMW, ST_F32, true) : FORGE_L(OP_ADAMW, ST_BF16, true);
@@ -462,6 +466,130 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
     return from_cuda(e);
 }
 
+// A multi-problem call: P problems share X [K, N]; problem j has dY_j
+// [K, M_j] and W_j, m_j, v_j [N, M_j].  One launch of the CTA-pair kernel
+// walks all problems' tiles (problem by problem, d_out fastest), so small
+// problems fill the SMs that a lone call of theirs would leave idle and the
+// launch has one tail instead of P.  bf16 inputs, AdamW.  Operands whose rows
+// TMA cannot address are staged into one pool allocation first.
+forge_status run_multi(const void* X, int64_t N, int64_t K, int32_t P, const void* const* dY,
+                       forge_dtype state_dtype, Params p, cudaStream_t stream)
+{
+    DeviceInfo* dev = nullptr;
+    forge_status st = current_device(&dev);
+    if (st != FORGE_OK) return st;
+    constexpr int es = 2;  // bf16
+    const int64_t tiles_n = (N + BN - 1) / BN;
+    int64_t total = 0;
+    for (int j = 0; j < P; ++j) {
+        const int64_t tm = (p.M_of[j] + 2 * BM - 1) / (2 * BM);
+        p.tile_begin[j] = static_cast<int32_t>(total);
+        p.tiles_m_of[j] = static_cast<int32_t>(tm);
+        total += tm * tiles_n;
+        if (total > INT32_MAX) return FORGE_ERR_INVALID_ARG;
+    }
+    for (int j = P; j <= kMaxProblems; ++j)
+        p.tile_begin[j] = j == P ? static_cast<int32_t>(total) : INT32_MAX;
+
+    const uintptr_t sa = state_dtype == FORGE_BF16 ? 2 : 4;
+    const uintptr_t va = state_dtype == FORGE_BF16 ? 8 : 16;
+    bool vec = true;
+    for (int j = 0; j < P; ++j) {
+        if (!aligned(p.W_of[j], 4) || !aligned(p.s1_of[j], sa) || !aligned(p.s2_of[j], sa))
+            return FORGE_ERR_MISALIGNED;
+        vec = vec && p.M_of[j] % 4 == 0 && aligned(p.W_of[j], 16) && aligned(p.s1_of[j], va) &&
+              aligned(p.s2_of[j], va);
+    }
+    p.vec_ok = vec ? 1 : 0;
+
+    // operands TMA cannot address: padded copies with 16-byte rows
+    const void* opX = X;
+    int64_t ldX = N * es;
+    const void* opD[kMaxProblems] = {};
+    int64_t ldD[kMaxProblems] = {};
+    int gran[kMaxProblems + 1] = {};
+    int64_t need = 0;
+    if (K > 0) {
+        gran[kMaxProblems] = operand_path(X, N, es);
+        if (gran[kMaxProblems] < 0) return FORGE_ERR_MISALIGNED;
+        if (gran[kMaxProblems] > 0) need += (ldX + 15) / 16 * 16 * K;
+        for (int j = 0; j < P; ++j) {
+            opD[j] = dY[j];
+            ldD[j] = p.M_of[j] * es;
+            gran[j] = operand_path(dY[j], p.M_of[j], es);
+            if (gran[j] < 0) return FORGE_ERR_MISALIGNED;
+            if (gran[j] > 0) need += (ldD[j] + 15) / 16 * 16 * K;
+        }
+    }
+    void* scratch = nullptr;
+    if (need > 0) {
+        if (scratch_alloc(&scratch, static_cast<size_t>(need), stream) != cudaSuccess) {
+            cudaGetLastError();
+            return FORGE_ERR_CUDA;
+        }
+        uint8_t* sp = static_cast<uint8_t*>(scratch);
+        cudaError_t ce = cudaSuccess;
+        if (gran[kMaxProblems] > 0) {
+            const int64_t pad = (ldX + 15) / 16 * 16;
+            ce = stage_rows(X, sp, K, ldX, pad, gran[kMaxProblems], dev->sms, stream);
+            opX = sp;
+            ldX = pad;
+            sp += pad * K;
+        }
+        for (int j = 0; j < P && ce == cudaSuccess; ++j) {
+            if (gran[j] == 0) continue;
+            const int64_t pad = (ldD[j] + 15) / 16 * 16;
+            ce = stage_rows(dY[j], sp, K, ldD[j], pad, gran[j], dev->sms, stream);
+            opD[j] = sp;
+            ldD[j] = pad;
+            sp += pad * K;
+        }
+        if (ce != cudaSuccess) {
+            scratch_free(scratch, stream);
+            return FORGE_ERR_CUDA;
+        }
+    }
+
+    Maps maps;
+    std::memset(&maps, 0, sizeof maps);
+    MultiMaps mm;
+    std::memset(&mm, 0, sizeof mm);
+    p.has_maps = K > 0 ? 1 : 0;
+    if (K > 0) {
+        st = encode_operand(&maps.b, opX, FORGE_BF16, N, K, ldX);
+        for (int j = 0; j < P && st == FORGE_OK; ++j)
+            st = encode_operand(&mm.a[j], opD[j], FORGE_BF16, p.M_of[j], K, ldD[j]);
+        if (st != FORGE_OK) {
+            if (scratch) scratch_free(scratch, stream);
+            return st;
+        }
+    }
+    p.N = N;
+    p.K = K;
+    p.E = 1;
+    p.P = P;
+    p.M = p.M_of[0];
+    p.W = p.W_of[0];
+    p.s1 = p.s1_of[0];
+    p.s2 = p.s2_of[0];
+    p.tiles_m = p.tiles_m_of[0];
+    p.tiles_n = static_cast<int32_t>(tiles_n);
+    p.raster_band = p.tiles_m;
+    p.timeout_ns = wait_timeout_ns();
+    p.status = dev->status;
+    cudaError_t e =
+        state_dtype == FORGE_BF16
+            ? launch_wgrad_pair<IN_BF16, OP_ADAMW, ST_BF16, 1, false, true>(
+                  maps.a, maps.b, maps.a1, maps.b1, maps.ak, maps.bk, mm, p, total, stream)
+            : launch_wgrad_pair<IN_BF16, OP_ADAMW, ST_F32, 1, false, true>(
+                  maps.a, maps.b, maps.a1, maps.b1, maps.ak, maps.bk, mm, p, total, stream);
+    if (scratch) {
+        const cudaError_t fe = scratch_free(scratch, stream);
+        if (e == cudaSuccess) e = fe;
+    }
+    return from_cuda(e);
+}
+
 forge_status check_sizes(int64_t M, int64_t N, int64_t K)
 {
     if (M < 1 || N < 1 || K < 0) return FORGE_ERR_INVALID_ARG;
@@ -615,6 +743,31 @@ forge_status forge_wgrad_adamw(const void* X, const void* dY, float* W, void* m,
     fill_adam(p, lr, beta1, beta2, eps, wd, step);
     return run(X, dY, K, in_dtype, OP_ADAMW, state_dtype, false, p,
                reinterpret_cast<cudaStream_t>(stream));
+}
+
+forge_status forge_wgrad_adamw_multi(const void* X, int64_t N, int64_t K, int32_t P,
+                                     const void* const* dY, const int64_t* M, float* const* W,
+                                     void* const* m, void* const* v, forge_dtype in_dtype,
+                                     forge_dtype state_dtype, float lr, float beta1, float beta2,
+                                     float eps, float wd, int64_t step, forge_stream_t stream)
+{
+    if (P < 1 || P > kMaxProblems || !M || !W || !m || !v || (K > 0 && (!X || !dY)))
+        return FORGE_ERR_INVALID_ARG;
+    if (in_dtype != FORGE_BF16) return FORGE_ERR_UNSUPPORTED_DTYPE;
+    if (state_dtype != FORGE_F32 && state_dtype != FORGE_BF16) return FORGE_ERR_UNSUPPORTED_DTYPE;
+    forge_status s;
+    if ((s = check_adam(lr, beta1, beta2, eps, wd, step)) != FORGE_OK) return s;
+    Params p{};
+    for (int j = 0; j < P; ++j) {
+        if ((s = check_sizes(M[j], N, K)) != FORGE_OK) return s;
+        if (!W[j] || !m[j] || !v[j] || (K > 0 && !dY[j])) return FORGE_ERR_INVALID_ARG;
+        p.M_of[j] = M[j];
+        p.W_of[j] = W[j];
+        p.s1_of[j] = m[j];
+        p.s2_of[j] = v[j];
+    }
+    fill_adam(p, lr, beta1, beta2, eps, wd, step);
+    return run_multi(X, N, K, P, dY, state_dtype, p, reinterpret_cast<cudaStream_t>(stream));
 }
 
 forge_status forge_wgrad_adamw_noalloc(const void* X, const void* dY, float* W, void* m, void* v,

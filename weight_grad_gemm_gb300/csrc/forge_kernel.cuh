@@ -52,6 +52,7 @@ constexpr int kStageB = 32768;  // BK rows x 256 n x elemsize
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kTmemCols = 512;  // two 256-column accumulators
 constexpr int kMaxExperts = 1024;
+constexpr int kMaxProblems = 8;  // multi-problem calls: problems sharing X per launch
 
 // Epilogue geometry for EW epilogue warps.  Warp (q, grp) owns TMEM lane
 // quarter q and warp_cols accumulator columns, walked in chunks of
@@ -150,12 +151,42 @@ struct Params {
     float lr, mu, wd;
     int64_t timeout_ns;
     int* status;  // device status word
+    // Multi-problem calls (P > 0): problems j = 0 .. P-1 share X, N and K and
+    // each has its own dY [K, M_of[j]] and W, m, v [N, M_of[j]]; problem j's
+    // tiles are [tile_begin[j], tile_begin[j + 1]) of the list, d_out fastest
+    // over tiles_m_of[j] tile rows.  Entries past P hold tile_begin = INT32_MAX.
+    int32_t P;
+    int32_t tile_begin[kMaxProblems + 1];
+    int32_t tiles_m_of[kMaxProblems];
+    int64_t M_of[kMaxProblems];
+    float* W_of[kMaxProblems];
+    void* s1_of[kMaxProblems];
+    void* s2_of[kMaxProblems];
 };
+
+// The dY tensor maps of a multi-problem call, one per problem.
+struct MultiMaps {
+    CUtensorMap a[kMaxProblems];
+};
+
+// Problem j's entry of a per-problem array of Params, by compile-time
+// indices only (select chain), so the parameter array is never indexed at
+// run time.
+template <class T, int LEN>
+__device__ __forceinline__ T pick(const T (&arr)[LEN], int32_t j)
+{
+    T r = arr[0];
+#pragma unroll
+    for (int i = 1; i < LEN; ++i)
+        if (j == i) r = arr[i];
+    return r;
+}
 
 struct Tile {
     int32_t m0, n0;
     int64_t k_begin, k_end;  // token rows [k_begin, k_end) of X / dY
     int64_t pbase;           // element offset of this tile's expert block in W / m / v
+    int32_t prob;            // multi-problem calls: the tile's problem
 };
 
 // Static tile list.  Dense: tiles ordered m-fastest so the CTAs of one wave
@@ -190,11 +221,29 @@ struct Sched {
     }
     const int32_t* offs;   // smem copy of offsets (grouped) or null
     const int32_t* order;  // smem expert order (grouped) or null
+    const Params* multi;   // the launch's parameters for a multi-problem call, else null
     int64_t K, MN;
 
     __device__ __forceinline__ Tile get(int32_t t) const
     {
         Tile r;
+        r.prob = 0;
+        if (multi) {
+            // problem j holds tiles [tile_begin[j], tile_begin[j + 1])
+            const Params& q = *multi;
+            int32_t j = 0;
+#pragma unroll
+            for (int i = 1; i < kMaxProblems; ++i) j += t >= q.tile_begin[i] ? 1 : 0;
+            const int32_t local = t - pick(q.tile_begin, j);
+            const int32_t tm = pick(q.tiles_m_of, j);
+            r.m0 = (local % tm) * m_step + m_off;
+            r.n0 = (local / tm) * BN;
+            r.k_begin = 0;
+            r.k_end = K;
+            r.pbase = 0;
+            r.prob = j;
+            return r;
+        }
         int32_t j = t / per_expert;
         int32_t local = t - j * per_expert;
         // Raster: bands of `band` d_out tiles; within a band, d_out fastest,
@@ -401,7 +450,7 @@ __device__ __forceinline__ void quad_transpose(float (&x)[4 * CN], int lane)
     }
 }
 
-template <int IT, int OP, int ST, class EC, class ReleaseAcc>
+template <int IT, int OP, int ST, class EC, bool MULTI = false, class ReleaseAcc>
 __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc,
                                               uint64_t* tfull, uint32_t tmem_base,
                                               volatile int* abort_flag, int warp, int lane,
@@ -417,7 +466,6 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc,
     using Chunk = forge::Chunk<kChunkN>;
     const int mg = lane >> 2;  // m group: lanes 4 mg .. 4 mg + 3 read TMEM rows 4 mg ..
     const int ns = lane & 3;   // n group within the chunk after the quad transpose
-    const int64_t M = p.M;
     const int64_t N = p.N;
     float gscale = 1.0f;
     if constexpr (IT == IN_E4M3) gscale = p.scales[0] * p.scales[1];
@@ -425,6 +473,11 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc,
     for (int32_t it = 0; it < sc.count; ++it) {
         const int32_t t = sc.nth(it);
         const Tile tl = sc.get(t);
+        // the tile's d_out and state (per problem in a multi-problem call)
+        const int64_t M = MULTI ? pick(p.M_of, tl.prob) : p.M;
+        float* const Wst = MULTI ? pick(p.W_of, tl.prob) : p.W;
+        void* const S1 = MULTI ? pick(p.s1_of, tl.prob) : p.s1;
+        void* const S2 = MULTI ? pick(p.s2_of, tl.prob) : p.s2;
         const bool has_acc = tl.k_end > tl.k_begin;
         const uint32_t b = ct & 1u;
         if (has_acc) {
@@ -484,16 +537,16 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc,
                     float* a = ch.a + 4 * jj;
                     float* bb = ch.b + 4 * jj;
                     if (vec) {
-                        StateIO<ST_F32>::ld4(p.W, idx, w);
-                        StateIO<ST>::ld4(p.s1, idx, a);
-                        if constexpr (OP == OP_ADAMW) StateIO<ST>::ld4(p.s2, idx, bb);
+                        StateIO<ST_F32>::ld4(Wst, idx, w);
+                        StateIO<ST>::ld4(S1, idx, a);
+                        if constexpr (OP == OP_ADAMW) StateIO<ST>::ld4(S2, idx, bb);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
                             if (i < mvalid) {
-                                w[i] = StateIO<ST_F32>::ld(p.W, idx + i);
-                                a[i] = StateIO<ST>::ld(p.s1, idx + i);
-                                if constexpr (OP == OP_ADAMW) bb[i] = StateIO<ST>::ld(p.s2, idx + i);
+                                w[i] = StateIO<ST_F32>::ld(Wst, idx + i);
+                                a[i] = StateIO<ST>::ld(S1, idx + i);
+                                if constexpr (OP == OP_ADAMW) bb[i] = StateIO<ST>::ld(S2, idx + i);
                             }
                     }
                 }
@@ -521,16 +574,16 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc,
                     float* bb = ch.b + 4 * jj;
                     step4<OP>(p, g, w, a, bb);
                     if (vec) {
-                        StateIO<ST_F32>::st4(p.W, idx, w);
-                        StateIO<ST>::st4(p.s1, idx, a);
-                        if constexpr (OP == OP_ADAMW) StateIO<ST>::st4(p.s2, idx, bb);
+                        StateIO<ST_F32>::st4(Wst, idx, w);
+                        StateIO<ST>::st4(S1, idx, a);
+                        if constexpr (OP == OP_ADAMW) StateIO<ST>::st4(S2, idx, bb);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
                             if (i < mvalid) {
-                                StateIO<ST_F32>::st(p.W, idx + i, w[i]);
-                                StateIO<ST>::st(p.s1, idx + i, a[i]);
-                                if constexpr (OP == OP_ADAMW) StateIO<ST>::st(p.s2, idx + i, bb[i]);
+                                StateIO<ST_F32>::st(Wst, idx + i, w[i]);
+                                StateIO<ST>::st(S1, idx + i, a[i]);
+                                if constexpr (OP == OP_ADAMW) StateIO<ST>::st(S2, idx + i, bb[i]);
                             }
                     }
                 }
@@ -757,6 +810,7 @@ __global__ void __launch_bounds__(EpiFor<GROUPED>::threads, 1)
     sc.set_share(blockIdx.x, gridDim.x, GROUPED ? 1 : 0);
     sc.offs = GROUPED ? s_offs : nullptr;
     sc.order = GROUPED ? s_order : nullptr;
+    sc.multi = nullptr;
     sc.K = p.K;
     sc.MN = p.M * p.N;
 
@@ -996,7 +1050,7 @@ constexpr int kPairStageBytes = kPairStageA + kPairStageB;
 using SmemPair = SmemLayout<kPairStages * kPairStageBytes>;
 static_assert(SmemPair::alloc(kCarveoutExperts) + 1024 <= kCarveout196, "196 KB step");
 
-template <int IT, int OP, int ST, int NPAIR, bool GROUPED>
+template <int IT, int OP, int ST, int NPAIR, bool GROUPED, bool MULTI>
 __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUPED>::threads, 1)
     forge_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,   // dY
                             const __grid_constant__ CUtensorMap tmB,   // X, boxes of BK / NPAIR rows
@@ -1004,10 +1058,12 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
                             const __grid_constant__ CUtensorMap tmB1,  // X, one-row boxes (grouped)
                             const __grid_constant__ CUtensorMap tmAk,  // dY, one-k-step boxes (grouped)
                             const __grid_constant__ CUtensorMap tmBk,  // X, one-k-step boxes (grouped)
-                            const Params p)
+                            const __grid_constant__ MultiMaps mm,      // dY of each problem (multi)
+                            const __grid_constant__ Params p)
 {
     static_assert(NPAIR == 1 || NPAIR == 2, "one or two pairs per cluster");
     static_assert(!GROUPED || NPAIR == 1, "grouped calls use single pairs");
+    static_assert(!MULTI || (NPAIR == 1 && !GROUPED), "multi-problem calls: single pairs, dense");
     static_assert(InTraits<IT>::BK == 4 * InTraits<IT>::umma_k,
                   "the one-k-step maps hold a quarter of a k-block");
     using TR = InTraits<IT>;
@@ -1064,7 +1120,11 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
         if (!grouped_setup(p, s_offs, s_order, abort_flag + 1)) return;
     }
     if (warp == 0 && lane == 0 && p.has_maps) {
-        ptx::prefetch_tensormap(&tmA);
+        if constexpr (MULTI) {
+            for (int j = 0; j < p.P; ++j) ptx::prefetch_tensormap(&mm.a[j]);
+        } else {
+            ptx::prefetch_tensormap(&tmA);
+        }
         ptx::prefetch_tensormap(&tmB);
     }
     if (warp == 1) {
@@ -1083,10 +1143,11 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
     sc.m_off = static_cast<int32_t>(crank) * BM;
     sc.band = p.raster_band;
     sc.per_expert = p.tiles_m * p.tiles_n;
-    sc.total = sc.per_expert * p.E;
+    sc.total = MULTI ? pick(p.tile_begin, p.P) : sc.per_expert * p.E;
     sc.set_share(blockIdx.x / (2 * NPAIR), gridDim.x / (2 * NPAIR), GROUPED ? 1 : 0);
     sc.offs = GROUPED ? s_offs : nullptr;
     sc.order = GROUPED ? s_order : nullptr;
+    sc.multi = MULTI ? &p : nullptr;
     sc.K = p.K;
     sc.MN = p.M * p.N;
 
@@ -1160,9 +1221,16 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
                             }
                         }
                     } else {
+                        // dY's map: the call's, or the tile's problem's
+                        const CUtensorMap* mapA = &tmA;
+                        if constexpr (MULTI) {
+#pragma unroll
+                            for (int j = 0; j < kMaxProblems; ++j)
+                                if (tl.prob == j) mapA = &mm.a[j];
+                        }
 #pragma unroll
                         for (int i = 0; i < kABoxes; ++i)
-                            ptx::tma_load_2d_pair_hint(sa + i * kBoxBytes, &tmA, bar,
+                            ptx::tma_load_2d_pair_hint(sa + i * kBoxBytes, mapA, bar,
                                                        tl.m0 + i * TR::box_mn, ky, pol);
 #pragma unroll
                         for (int i = 0; i < kBBoxes; ++i) {
@@ -1258,7 +1326,7 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
         }
     } else if (warp >= kEpiWarp0) {
         const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), lead_rank);
-        epilogue_role<IT, OP, ST, EpiFor<GROUPED>>(
+        epilogue_role<IT, OP, ST, EpiFor<GROUPED>, MULTI>(
             p, sc, tfull, tmem_base, abort_flag, warp, lane, [&](uint32_t b) {
                                       if (leader)
                                           ptx::mbar_arrive(&tempty[b]);

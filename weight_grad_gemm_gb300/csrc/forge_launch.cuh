@@ -18,27 +18,29 @@ cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB, const C
 // Same for the CTA-pair kernels.  The grid is sized from the number of
 // clusters of 2 * NPAIR CTAs that can be resident at once (a cluster must fit
 // in one GPC), never more than `total_tiles` clusters.
-template <int IT, int OP, int ST, int NPAIR, bool GROUPED>
+template <int IT, int OP, int ST, int NPAIR, bool GROUPED, bool MULTI>
 cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                               const CUtensorMap& tmA1, const CUtensorMap& tmB1,
-                              const CUtensorMap& tmAk, const CUtensorMap& tmBk, const Params& p,
-                              int64_t total_tiles, cudaStream_t stream);
+                              const CUtensorMap& tmAk, const CUtensorMap& tmBk,
+                              const MultiMaps& mm, const Params& p, int64_t total_tiles,
+                              cudaStream_t stream);
 
 }  // namespace forge
 
 #define FORGE_DEFINE_LAUNCH_PAIR()                                                             \
     namespace forge {                                                                          \
-    template <int IT, int OP, int ST, int NPAIR, bool GROUPED>                                 \
+    template <int IT, int OP, int ST, int NPAIR, bool GROUPED, bool MULTI>                     \
     cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,              \
                                   const CUtensorMap& tmA1, const CUtensorMap& tmB1,            \
                                   const CUtensorMap& tmAk, const CUtensorMap& tmBk,            \
-                                  const Params& p, int64_t total_tiles, cudaStream_t stream)   \
+                                  const MultiMaps& mm, const Params& p, int64_t total_tiles,   \
+                                  cudaStream_t stream)                                         \
     {                                                                                          \
         static int max_clusters[64] = {0};                                                     \
         int dev = 0;                                                                           \
         cudaError_t e = cudaGetDevice(&dev);                                                   \
         if (e != cudaSuccess) return e;                                                        \
-        auto kern = forge_wgrad_pair_kernel<IT, OP, ST, NPAIR, GROUPED>;                       \
+        auto kern = forge_wgrad_pair_kernel<IT, OP, ST, NPAIR, GROUPED, MULTI>;                \
         int& mc = max_clusters[dev & 63];                                                      \
         if (__atomic_load_n(&mc, __ATOMIC_ACQUIRE) == 0) {                                     \
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
@@ -57,15 +59,15 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
         const int64_t nc = total_tiles < mc ? total_tiles : mc;                                \
         kern<<<static_cast<int>(2 * NPAIR * nc), EpiFor<GROUPED>::threads, SmemPair::alloc(p.E), \
                stream>>>(                                                                      \
-            tmA, tmB, tmA1, tmB1, tmAk, tmBk, p);                                              \
+            tmA, tmB, tmA1, tmB1, tmAk, tmBk, mm, p);                                          \
         return cudaGetLastError();                                                             \
     }                                                                                          \
     }
 
-#define FORGE_INSTANTIATE_PAIR(IT, OP, ST, NPAIR, G)                                           \
-    template cudaError_t forge::launch_wgrad_pair<IT, OP, ST, NPAIR, G>(                       \
+#define FORGE_INSTANTIATE_PAIR(IT, OP, ST, NPAIR, G, MU)                                       \
+    template cudaError_t forge::launch_wgrad_pair<IT, OP, ST, NPAIR, G, MU>(                   \
         const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,        \
-        const CUtensorMap&, const CUtensorMap&,                                                \
+        const CUtensorMap&, const CUtensorMap&, const forge::MultiMaps&,                       \
         const forge::Params&, int64_t, cudaStream_t);
 
 #define FORGE_DEFINE_LAUNCH()                                                                  \
