@@ -89,3 +89,15 @@ def test_multi_run_to_run_bitwise(cuda_device):
     b = run_multi(cuda_device, X, Ds, states, step=4)
     for x, y in zip(a, b):
         assert all(np.array_equal(u, w) for u, w in zip(x, y))
+
+
+def test_multi_with_staged_x(cuda_device):
+    # d_in 262: X rows of 524 bytes, staged into 16-byte rows along with the
+    # 260-byte dY rows of the 130-wide problem
+    K, N = 150, 262
+    Ms = [264, 130, 64]
+    X, Ds, states = case(K, N, Ms, 35, False)
+    got = run_multi(cuda_device, X, Ds, states, step=2)
+    for D, (W, m, v), g in zip(Ds, states, got):
+        G = oracle.wgrad(X, D)
+        check_adamw(g, oracle.adamw(G, W, m, v, step=2, **vars(HP)), G, HP.lr, False)

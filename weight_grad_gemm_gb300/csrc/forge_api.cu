@@ -28,7 +28,8 @@ namespace {
 using namespace forge;
 
 constexpr int kMaxDevices = 64;
-constexpr int32_t kDefaultRasterBand = 0;  // plain d_out-fastest order
+constexpr int32_t kDefaultRasterBand = 0;         // dense: plain d_out-fastest order
+constexpr int32_t kDefaultGroupedRasterBand = 8;  // grouped: bands of 8 d_out tiles
 
 // Device status word: 0, or the first device-side error since the last read.
 __device__ int g_forge_status = 0;
@@ -289,9 +290,13 @@ int kernel_form(const Params& p, bool grouped, bool manual)
 
 // d_out tiles per raster band.  FORGE_RASTER_BAND (read on every call)
 // overrides the default; 0 or a value >= tiles_m means plain d_out-fastest.
-int32_t raster_band(int32_t tiles_m)
+int32_t raster_band(int32_t tiles_m, bool grouped)
 {
-    int32_t band = kDefaultRasterBand;
+    // Grouped calls walk their tile list from both ends, so two experts'
+    // operands are live at once; bands of 8 d_out tiles keep each wave's dY
+    // columns fewer (MoE layer: 1.9% faster over the six routings than the
+    // plain order, 4 slower again).  Dense calls measured no gain from bands.
+    int32_t band = grouped ? kDefaultGroupedRasterBand : kDefaultRasterBand;
     if (const char* e = std::getenv("FORGE_RASTER_BAND")) band = std::atoi(e);
     if (band <= 0 || band > tiles_m) band = tiles_m;
     return band;
@@ -433,7 +438,7 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
     const int64_t total = tiles_m * tiles_n * p.E;  // at least 1, within the bound checked above
     p.tiles_m = static_cast<int32_t>(tiles_m);
     p.tiles_n = static_cast<int32_t>(tiles_n);
-    p.raster_band = raster_band(p.tiles_m);
+    p.raster_band = raster_band(p.tiles_m, grouped);
     p.timeout_ns = wait_timeout_ns();
     p.status = dev->status;
 
