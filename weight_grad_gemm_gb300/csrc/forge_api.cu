@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -579,7 +580,9 @@ forge_status run_multi(const void* X, int64_t N, int64_t K, int32_t P, const voi
     p.s2 = p.s2_of[0];
     p.tiles_m = p.tiles_m_of[0];
     p.tiles_n = static_cast<int32_t>(tiles_n);
-    p.raster_band = p.tiles_m;
+    int32_t tm_max = 1;
+    for (int j = 0; j < P; ++j) tm_max = std::max(tm_max, p.tiles_m_of[j]);
+    p.raster_band = raster_band(tm_max, false);
     p.timeout_ns = wait_timeout_ns();
     p.status = dev->status;
     cudaError_t e =

@@ -236,8 +236,15 @@ struct Sched {
             for (int i = 1; i < kMaxProblems; ++i) j += t >= q.tile_begin[i] ? 1 : 0;
             const int32_t local = t - pick(q.tile_begin, j);
             const int32_t tm = pick(q.tiles_m_of, j);
-            r.m0 = (local % tm) * m_step + m_off;
-            r.n0 = (local / tm) * BN;
+            // the problem's tiles in raster bands, as below
+            const int32_t bw = band < tm ? band : tm;
+            const int32_t per_band = bw * tiles_n;
+            const int32_t g = local / per_band;
+            const int32_t within = local - g * per_band;
+            const int32_t rows_left = tm - g * bw;
+            const int32_t gsz = rows_left < bw ? rows_left : bw;
+            r.m0 = (g * bw + within % gsz) * m_step + m_off;
+            r.n0 = (within / gsz) * BN;
             r.k_begin = 0;
             r.k_end = K;
             r.pbase = 0;
