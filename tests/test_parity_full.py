@@ -94,6 +94,39 @@ def test_attention_projections_full_size(cuda_device, idx, state):
 
 
 @pytest.mark.parametrize("state", ["f32", "bf16"])
+def test_attention_set_one_launch_full_size(cuda_device, state):
+    """The four projections as the benchmark runs them: one multi-problem
+    call over the shared X (K 16384, d_in 4096, d_out 4096/1024/1024/4100),
+    step 1 warming m, v from zero, step 2 checked on sampled rows of every
+    problem."""
+    dev = cuda_device
+    sd = torch.float32 if state == "f32" else torch.bfloat16
+    wks = wl.ATTN_PROJ
+    K, N = wks[0].K, wks[0].N
+    hp = wks[0].adam.f32()
+    Ws = [wl.randn((N, wk.M), wl.seed_of(wk.name, "W"), device=dev, std=0.02) for wk in wks]
+    ms = [torch.zeros((N, wk.M), dtype=sd, device=dev) for wk in wks]
+    vs = [torch.zeros((N, wk.M), dtype=sd, device=dev) for wk in wks]
+    rows = sample_rows(N)
+    for t in (1, 2):
+        X = wl.activations(K, N, wl.seed_of("attn_set", "X", t), device=dev)
+        Ds = [wl.activations(K, wk.M, wl.seed_of(wk.name, "dY", t), device=dev) for wk in wks]
+        if t == 2:
+            before = [tuple(state_host(a[rows]) for a in s3) for s3 in zip(Ws, ms, vs)]
+        fg.forge_wgrad_adamw_multi(X, Ds, Ws, ms, vs, lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2,
+                                   eps=hp.eps, wd=hp.wd, step=t)
+    torch.cuda.synchronize()
+    assert fg.forge_get_device_status() == fg.FORGE_OK
+    Xh = host(X)
+    for j, D in enumerate(Ds):
+        W0, m0, v0 = before[j]
+        G = oracle.wgrad(Xh, host(D), rows=rows)
+        ref = oracle.adamw(G, W0, m0, v0, step=2, **vars(hp))
+        check_rows(state_host(Ws[j][rows]), state_host(ms[j][rows]), state_host(vs[j][rows]),
+                   ref, G, hp.lr, state == "bf16", m0=m0, beta1=hp.beta1)
+
+
+@pytest.mark.parametrize("state", ["f32", "bf16"])
 def test_moe_grouped_full_size(cuda_device, state):
     """8 experts of [14336, 4096]; step 2 of the routed workload, on which 4
     seeded experts receive no tokens (their m, v decay exactly by beta)."""
