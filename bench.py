@@ -484,11 +484,11 @@ WORKLOADS = {
 
 # ---------------------------------------------------------------- CPU oracle leg
 
-def oracle_sample(job_X, job_D, job_W, job_m, job_v, hp, step, rows):
+def oracle_sample(job_X, job_D, job_W, job_m, job_v, hp, step, rows, scales=(1.0, 1.0)):
     """The oracle (fp64 CPU) on `rows` output rows of the workload: the
     contraction over all K for those rows and the AdamW step on them."""
     import oracle
-    G = oracle.wgrad(job_X, job_D, rows=rows)
+    G = oracle.wgrad(job_X, job_D, rows=rows, scales=scales)
     oracle.adamw(G, job_W[rows], job_m[rows], job_v[rows], lr=hp.lr, beta1=hp.beta1,
                  beta2=hp.beta2, eps=hp.eps, wd=hp.wd, step=step)
 
@@ -533,18 +533,29 @@ def run_reference(args):
         return 0
     import oracle
     oracle.build()
-    wk = {"mlp_down": wl.MLP_DOWN, "attn_proj": wl.ATTN_PROJ[0], "linear": wl.LINEAR}[args.workload]
-    K, N, M = wk.K, wk.N, wk.M
+    # the contraction each workload times: the attention set by its widest
+    # projection, the MoE layers by one expert of their average token count,
+    # the fp8 workloads with e4m3 inputs and their scales
+    wk = {"mlp_down": wl.MLP_DOWN, "backward": wl.MLP_DOWN, "attn_proj": wl.ATTN_PROJ[0],
+          "linear": wl.LINEAR, "fp8": wl.FP8, "fp8_sgdm": wl.FP8, "fp8_quant": wl.FP8,
+          "moe": wl.MOE, "moe_small": wl.MOE_SMALL}[args.workload]
+    K, N, M = wk.K // max(wk.experts, 1), wk.N, wk.M
     hp = wk.adam.f32()
-    X = oracle.as_bits(wl.activations(K, N, wl.seed_of(wk.name, "X")))
-    D = oracle.as_bits(wl.activations(K, M, wl.seed_of(wk.name, "dY")))
+    scales = (1.0, 1.0)
+    if wk is wl.FP8:
+        Xq, sx = wl.quantize_e4m3(wl.with_outliers((K, N), wl.seed_of(wk.name, "X8")))
+        Dq, sy = wl.quantize_e4m3(wl.with_outliers((K, M), wl.seed_of(wk.name, "dY8")))
+        X, D, scales = oracle.as_bits(Xq), oracle.as_bits(Dq), (sx, sy)
+    else:
+        X = oracle.as_bits(wl.activations(K, N, wl.seed_of(wk.name, "X")))
+        D = oracle.as_bits(wl.activations(K, M, wl.seed_of(wk.name, "dY")))
     rng = np.random.default_rng(0)
     # state rows only for the sampled output rows (the rest is never touched)
     total_budget_s = 150.0
     t0 = time.perf_counter()
     oracle_sample(X, D, (rng.standard_normal((1, M)) * 0.02).astype(np.float32),
                   np.zeros((1, M), np.float32), np.zeros((1, M), np.float32), hp, wk.first_step,
-                  [0])
+                  [0], scales)
     t1 = max(time.perf_counter() - t0, 1e-4)
     rows_per_step = int(max(1, min(N, total_budget_s / (args.steps + args.warmup) / t1)))
     Wr = (rng.standard_normal((rows_per_step, M)) * 0.02).astype(np.float32)
@@ -552,10 +563,10 @@ def run_reference(args):
     vr = (rng.standard_normal((rows_per_step, M)) * 1e-3).astype(np.float32) ** 2
     rows = list(range(rows_per_step))
     for _ in range(args.warmup):
-        oracle_sample(X, D, Wr, mr, vr, hp, wk.first_step, rows)
+        oracle_sample(X, D, Wr, mr, vr, hp, wk.first_step, rows, scales)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_sample(X, D, Wr, mr, vr, hp, wk.first_step, rows)
+        oracle_sample(X, D, Wr, mr, vr, hp, wk.first_step, rows, scales)
     dt = (time.perf_counter() - t0) / args.steps
     value = 2.0 * rows_per_step * M * K / dt / 1e12
     cores = len(os.sched_getaffinity(0))
@@ -564,7 +575,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wk.name, "sample_rows_per_step": rows_per_step},
+        "config": {"workload": wk.name, "K": K, "d_in": N, "d_out": M,
+                   "sample_rows_per_step": rows_per_step},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{rows_per_step} of {N} output rows per step (all {M} "
                                    f"columns, full K={K}) of dW + AdamW"},
