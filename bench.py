@@ -493,6 +493,28 @@ def oracle_sample(job_X, job_D, job_W, job_m, job_v, hp, step, rows, scales=(1.0
                  beta2=hp.beta2, eps=hp.eps, wd=hp.wd, step=step)
 
 
+def oracle_case(workload):
+    """The contraction the oracle times for a workload, on host copies of
+    seeded inputs: the attention set by its widest projection, the MoE
+    layers by one expert of their average token count, the fp8 workloads
+    with e4m3 inputs and their scales.  Returns (workload spec, X, dY,
+    scales, K, N, M)."""
+    import oracle
+    wk = {"mlp_down": wl.MLP_DOWN, "backward": wl.MLP_DOWN, "attn_proj": wl.ATTN_PROJ[0],
+          "linear": wl.LINEAR, "fp8": wl.FP8, "fp8_sgdm": wl.FP8, "fp8_quant": wl.FP8,
+          "moe": wl.MOE, "moe_small": wl.MOE_SMALL}[workload]
+    K, N, M = wk.K // max(wk.experts, 1), wk.N, wk.M
+    scales = (1.0, 1.0)
+    if wk is wl.FP8:
+        Xq, sx = wl.quantize_e4m3(wl.with_outliers((K, N), wl.seed_of(wk.name, "X8")))
+        Dq, sy = wl.quantize_e4m3(wl.with_outliers((K, M), wl.seed_of(wk.name, "dY8")))
+        X, D, scales = oracle.as_bits(Xq), oracle.as_bits(Dq), (sx, sy)
+    else:
+        X = oracle.as_bits(wl.activations(K, N, wl.seed_of(wk.name, "X")))
+        D = oracle.as_bits(wl.activations(K, M, wl.seed_of(wk.name, "dY")))
+    return wk, X, D, scales, K, N, M
+
+
 def host_copies(job):
     import oracle
     X = oracle.as_bits(job.X.cpu())
@@ -503,20 +525,32 @@ def host_copies(job):
     return X, D, W, m, v
 
 
-def cpu_baseline(job, target_s=15.0):
+def cpu_baseline(job, workload, target_s=15.0):
+    """The oracle's rate on the host cores: a dense job's own inputs and
+    state, else the workload's oracle case (seeded inputs, warm state)."""
     import oracle
     oracle.build()
-    X, D, W, m, v = host_copies(job)
-    K, N, M = job.wk.K, job.wk.N, job.wk.M
-    oracle_sample(X, D, W, m, v, job.hp, job.t, list(range(2)))  # warm caches and threads
+    scales = (1.0, 1.0)
+    if type(job) is Dense:
+        X, D, W, m, v = host_copies(job)
+        K, N, M = job.wk.K, job.wk.N, job.wk.M
+        hp, t = job.hp, job.t
+    else:
+        wk, X, D, scales, K, N, M = oracle_case(workload)
+        rng = np.random.default_rng(0)
+        W = (rng.standard_normal((N, M)) * 0.02).astype(np.float32)
+        m = (rng.standard_normal((N, M)) * 1e-3).astype(np.float32)
+        v = (rng.standard_normal((N, M)) * 1e-3).astype(np.float32) ** 2
+        hp, t = wk.adam.f32(), 4
+    oracle_sample(X, D, W, m, v, hp, t, list(range(2)), scales)  # warm caches and threads
     rows = list(range(32))
     t0 = time.perf_counter()
-    oracle_sample(X, D, W, m, v, job.hp, job.t, rows)
+    oracle_sample(X, D, W, m, v, hp, t, rows, scales)
     t_cal = time.perf_counter() - t0
     n = int(max(32, min(N, 32 * target_s / max(t_cal, 1e-3))))
     rows = list(range(n))
     t0 = time.perf_counter()
-    oracle_sample(X, D, W, m, v, job.hp, job.t, rows)
+    oracle_sample(X, D, W, m, v, hp, t, rows, scales)
     dt = time.perf_counter() - t0
     flops = 2.0 * n * M * K
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
@@ -533,22 +567,8 @@ def run_reference(args):
         return 0
     import oracle
     oracle.build()
-    # the contraction each workload times: the attention set by its widest
-    # projection, the MoE layers by one expert of their average token count,
-    # the fp8 workloads with e4m3 inputs and their scales
-    wk = {"mlp_down": wl.MLP_DOWN, "backward": wl.MLP_DOWN, "attn_proj": wl.ATTN_PROJ[0],
-          "linear": wl.LINEAR, "fp8": wl.FP8, "fp8_sgdm": wl.FP8, "fp8_quant": wl.FP8,
-          "moe": wl.MOE, "moe_small": wl.MOE_SMALL}[args.workload]
-    K, N, M = wk.K // max(wk.experts, 1), wk.N, wk.M
+    wk, X, D, scales, K, N, M = oracle_case(args.workload)
     hp = wk.adam.f32()
-    scales = (1.0, 1.0)
-    if wk is wl.FP8:
-        Xq, sx = wl.quantize_e4m3(wl.with_outliers((K, N), wl.seed_of(wk.name, "X8")))
-        Dq, sy = wl.quantize_e4m3(wl.with_outliers((K, M), wl.seed_of(wk.name, "dY8")))
-        X, D, scales = oracle.as_bits(Xq), oracle.as_bits(Dq), (sx, sy)
-    else:
-        X = oracle.as_bits(wl.activations(K, N, wl.seed_of(wk.name, "X")))
-        D = oracle.as_bits(wl.activations(K, M, wl.seed_of(wk.name, "dY")))
     rng = np.random.default_rng(0)
     # state rows only for the sampled output rows (the rest is never touched)
     total_budget_s = 150.0
@@ -925,9 +945,8 @@ def main():
         line["quantize"] = {"us": q_us, "fused_us": f_us, "bound": "hbm", "achieved": gbs,
                             "peak": bw, "unit": "GB/s", "frac": gbs / bw,
                             "bytes": job.quant_bytes}
-    if (rank == 0 and world == 1 and not args.no_cpu_baseline and args.impl == "ours" and
-            type(job) is Dense):
-        line["cpu_baseline"] = cpu_baseline(job)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.impl == "ours":
+        line["cpu_baseline"] = cpu_baseline(job, args.workload)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
