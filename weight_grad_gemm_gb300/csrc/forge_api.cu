@@ -236,7 +236,8 @@ template <int IT, bool MAN>
 cudaError_t dispatch_op(int op, int st, bool grouped, const Maps& m, const Params& p, int grid,
                         cudaStream_t s)
 {
-#define FORGE_L(OPV, STV, G) launch_wgrad<IT, OPV, STV, G, MAN>(m.a, m.b, m.a1, m.b1, p, grid, s)
+#define FORGE_L(OPV, STV, G) \
+    launch_wgrad<IT, OPV, STV, G, MAN>(m.a, m.b, m.a1, m.b1, m.ak, m.bk, p, grid, s)
     if (grouped)
         return st == ST_F32 ? FORGE_L(OP_ADAMW, ST_F32, true) : FORGE_L(OP_ADAMW, ST_BF16, true);
     switch (op) {

@@ -664,24 +664,42 @@ __device__ __forceinline__ bool grouped_setup(const Params& p, int32_t* s_offs, 
     return true;
 }
 
-// A k-block that runs past the current expert's tokens (grouped calls):
-// rows [ky, ky + BK) of NBOX 128-byte column blocks from column mn0 are
-// fetched four at a time through a one-row-box map, each row at or past kend
-// replaced by the out-of-range index oob so that TMA writes zeros there.  Both
-// operands are loaded this way, so another expert's tokens never enter the
-// product (not even as 0 x inf).  issue(byte offset, column, rows[4]) makes
-// one copy.
-template <int BK, int NBOX, int BOX_MN, int BOX_BYTES, class Issue>
-__device__ __forceinline__ void gather_block(int32_t mn0, int32_t ky, int32_t kend, int32_t oob,
-                                             Issue&& issue)
+// An expert's last k-block (grouped calls): rows [ky, ky + BK) of NBOX
+// 128-byte column blocks from column mn0, of which the rows before kend
+// belong to the expert.  Rows at or past kend must read as zeros in both
+// operands, so that another expert's tokens never enter the product (not
+// even as 0 x inf).  The whole MMA k-steps of UK rows come as k-step-high
+// boxes, box(byte offset, column, row); the incomplete k-step four rows at a
+// time through a one-row-box map, gather(byte offset, column, rows[4]), rows
+// at or past kend given the out-of-range index oob (TMA writes zeros); the
+// k-steps after it as boxes starting at oob, past the tensor's last row
+// (zero filled).  The stage receives BK rows of bytes, as a full k-block.
+// Gathering the whole block four rows at a time took 16 copies per column
+// block and stalled the MMA issuer about 2.6 us on every tile.
+template <int BK, int UK, int NBOX, int BOX_MN, int BOX_BYTES, class Box, class Gather>
+__device__ __forceinline__ void partial_block(int32_t mn0, int32_t ky, int32_t kend, int32_t oob,
+                                              Box&& box, Gather&& gather)
 {
+    static_assert(BK % UK == 0 && UK % 4 == 0, "k-steps of whole four-row gathers");
+    const int32_t valid = kend - ky;
+    const int32_t whole = valid / UK;
+    const int32_t steps = (valid + UK - 1) / UK;
 #pragma unroll 1
-    for (int r = 0; r < BK; r += 4) {
-        int32_t y[4];
+    for (int32_t j = 0; j < BK / UK; ++j) {
+        if (j == whole && whole < steps) continue;  // gathered below
+        const int32_t y = j < whole ? ky + j * UK : oob;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) y[j] = ky + r + j < kend ? ky + r + j : oob;
+        for (int i = 0; i < NBOX; ++i) box(i * BOX_BYTES + j * UK * 128, mn0 + i * BOX_MN, y);
+    }
+    if (whole < steps) {
+#pragma unroll 1
+        for (int32_t r = whole * UK; r < steps * UK; r += 4) {
+            int32_t y[4];
 #pragma unroll
-        for (int i = 0; i < NBOX; ++i) issue(i * BOX_BYTES + r * 128, mn0 + i * BOX_MN, y);
+            for (int j = 0; j < 4; ++j) y[j] = ky + r + j < kend ? ky + r + j : oob;
+#pragma unroll
+            for (int i = 0; i < NBOX; ++i) gather(i * BOX_BYTES + r * 128, mn0 + i * BOX_MN, y);
+        }
     }
 }
 
@@ -746,6 +764,8 @@ __global__ void __launch_bounds__(EpiFor<GROUPED>::threads, 1)
                        const __grid_constant__ CUtensorMap tmB,   // X
                        const __grid_constant__ CUtensorMap tmA1,  // dY, one-row boxes (grouped)
                        const __grid_constant__ CUtensorMap tmB1,  // X, one-row boxes (grouped)
+                       const __grid_constant__ CUtensorMap tmAk,  // dY, one-k-step boxes (grouped)
+                       const __grid_constant__ CUtensorMap tmBk,  // X, one-k-step boxes (grouped)
                        const Params p)
 {
     using TR = InTraits<IT>;
@@ -851,8 +871,12 @@ __global__ void __launch_bounds__(EpiFor<GROUPED>::threads, 1)
                     const int32_t oob = static_cast<int32_t>(p.T_max);
                     if (tma_a) {
                         if (partial) {
-                            gather_block<BK, kABoxes, TR::box_mn, kBoxBytes>(
-                                tl.m0, ky, kend, oob, [&](int off, int32_t x, const int32_t* y) {
+                            partial_block<BK, TR::umma_k, kABoxes, TR::box_mn, kBoxBytes>(
+                                tl.m0, ky, kend, oob,
+                                [&](int off, int32_t x, int32_t y) {
+                                    ptx::tma_load_2d(sa + off, &tmAk, &full[s], x, y);
+                                },
+                                [&](int off, int32_t x, const int32_t* y) {
                                     ptx::tma_gather4_2d(sa + off, &tmA1, &full[s], x, y[0], y[1],
                                                         y[2], y[3]);
                                 });
@@ -865,8 +889,12 @@ __global__ void __launch_bounds__(EpiFor<GROUPED>::threads, 1)
                     }
                     if (tma_b) {
                         if (partial) {
-                            gather_block<BK, kBBoxes, TR::box_mn, kBoxBytes>(
-                                tl.n0, ky, kend, oob, [&](int off, int32_t x, const int32_t* y) {
+                            partial_block<BK, TR::umma_k, kBBoxes, TR::box_mn, kBoxBytes>(
+                                tl.n0, ky, kend, oob,
+                                [&](int off, int32_t x, int32_t y) {
+                                    ptx::tma_load_2d(sb + off, &tmBk, &full[s], x, y);
+                                },
+                                [&](int off, int32_t x, const int32_t* y) {
                                     ptx::tma_gather4_2d(sb + off, &tmB1, &full[s], x, y[0], y[1],
                                                         y[2], y[3]);
                                 });
@@ -1183,50 +1211,27 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
                     const int32_t ky = static_cast<int32_t>(k);
                     const int32_t nb = tl.n0 + static_cast<int32_t>(rank) * (BN / 2);
                     if (GROUPED && tl.k_end - k < BK) {
-                        // The expert's last k-block carries valid < BK token
-                        // rows.  Its whole MMA k-steps come as k-step-high
-                        // boxes; the incomplete one four rows at a time, rows
-                        // past the expert's end read as zeros; the k-steps
-                        // after it as boxes starting past the tensor's last
-                        // row, which TMA fills with zeros.  Every row of
-                        // another expert stays out of the product.
-                        const int32_t valid = static_cast<int32_t>(tl.k_end - k);
-                        const int32_t whole = valid / TR::umma_k;
-                        const int32_t steps = (valid + TR::umma_k - 1) / TR::umma_k;
+                        // the expert's last k-block: rows past its end read as zeros
+                        const int32_t kend = static_cast<int32_t>(tl.k_end);
                         const int32_t oob = static_cast<int32_t>(p.T_max);
-#pragma unroll 1
-                        for (int32_t j = 0; j < kKSteps; ++j) {
-                            if (j == whole && whole < steps) continue;  // gathered below
-                            const int off = j * TR::umma_k * 128;
-                            const int32_t y = j < whole ? ky + j * TR::umma_k : oob;
-#pragma unroll
-                            for (int i = 0; i < kABoxes; ++i)
-                                ptx::tma_load_2d_pair(sa + i * kBoxBytes + off, &tmAk, bar,
-                                                      tl.m0 + i * TR::box_mn, y);
-#pragma unroll
-                            for (int i = 0; i < kBBoxes; ++i)
-                                ptx::tma_load_2d_pair(sb + i * kBoxBytes + off, &tmBk, bar,
-                                                      nb + i * TR::box_mn, y);
-                        }
-                        if (whole < steps) {
-                            const int32_t kend = static_cast<int32_t>(tl.k_end);
-#pragma unroll 1
-                            for (int32_t r = whole * TR::umma_k; r < steps * TR::umma_k; r += 4) {
-                                int32_t y[4];
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) y[j] = ky + r + j < kend ? ky + r + j : oob;
-#pragma unroll
-                                for (int i = 0; i < kABoxes; ++i)
-                                    ptx::tma_gather4_2d_pair(sa + i * kBoxBytes + r * 128, &tmA1, bar,
-                                                             tl.m0 + i * TR::box_mn, y[0], y[1], y[2],
-                                                             y[3]);
-#pragma unroll
-                                for (int i = 0; i < kBBoxes; ++i)
-                                    ptx::tma_gather4_2d_pair(sb + i * kBoxBytes + r * 128, &tmB1, bar,
-                                                             nb + i * TR::box_mn, y[0], y[1], y[2],
-                                                             y[3]);
-                            }
-                        }
+                        partial_block<BK, TR::umma_k, kABoxes, TR::box_mn, kBoxBytes>(
+                            tl.m0, ky, kend, oob,
+                            [&](int off, int32_t x, int32_t y) {
+                                ptx::tma_load_2d_pair(sa + off, &tmAk, bar, x, y);
+                            },
+                            [&](int off, int32_t x, const int32_t* y) {
+                                ptx::tma_gather4_2d_pair(sa + off, &tmA1, bar, x, y[0], y[1],
+                                                         y[2], y[3]);
+                            });
+                        partial_block<BK, TR::umma_k, kBBoxes, TR::box_mn, kBoxBytes>(
+                            nb, ky, kend, oob,
+                            [&](int off, int32_t x, int32_t y) {
+                                ptx::tma_load_2d_pair(sb + off, &tmBk, bar, x, y);
+                            },
+                            [&](int off, int32_t x, const int32_t* y) {
+                                ptx::tma_gather4_2d_pair(sb + off, &tmB1, bar, x, y[0], y[1],
+                                                         y[2], y[3]);
+                            });
                     } else {
                         // dY's map: the call's, or the tile's problem's
                         const CUtensorMap* mapA = &tmA;

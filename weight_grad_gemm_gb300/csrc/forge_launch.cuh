@@ -13,7 +13,8 @@ namespace forge {
 // device) and launches it on `stream`.
 template <int IT, int OP, int ST, bool GROUPED, bool MANUAL>
 cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmA1,
-                         const CUtensorMap& tmB1, const Params& p, int grid, cudaStream_t stream);
+                         const CUtensorMap& tmB1, const CUtensorMap& tmAk,
+                         const CUtensorMap& tmBk, const Params& p, int grid, cudaStream_t stream);
 
 // Same for the CTA-pair kernels.  The grid is sized from the number of
 // clusters of 2 * NPAIR CTAs that can be resident at once (a cluster must fit
@@ -75,6 +76,7 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
     template <int IT, int OP, int ST, bool GROUPED, bool MANUAL>                               \
     cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB,                   \
                              const CUtensorMap& tmA1, const CUtensorMap& tmB1,                 \
+                             const CUtensorMap& tmAk, const CUtensorMap& tmBk,                 \
                              const Params& p, int grid, cudaStream_t stream)                   \
     {                                                                                          \
         static unsigned long long attr_done = 0; /* one bit per device ordinal < 64 */         \
@@ -90,8 +92,7 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
             __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);                              \
         }                                                                                      \
         kern<<<grid, EpiFor<GROUPED>::threads, SmemCta::alloc(p.E), stream>>>(                 \
-            tmA, tmB, tmA1, tmB1,                                                              \
-                                                                     p);                       \
+            tmA, tmB, tmA1, tmB1, tmAk, tmBk, p);                                              \
         return cudaGetLastError();                                                             \
     }                                                                                          \
     }
@@ -99,4 +100,4 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
 #define FORGE_INSTANTIATE(IT, OP, ST, G, MAN)                                                  \
     template cudaError_t forge::launch_wgrad<IT, OP, ST, G, MAN>(                              \
         const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,        \
-        const forge::Params&, int, cudaStream_t);
+        const CUtensorMap&, const CUtensorMap&, const forge::Params&, int, cudaStream_t);
