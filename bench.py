@@ -279,15 +279,18 @@ class AttnSet:
 class MoE:
     """Grouped call over 8 experts [14336, 4096]; the step cycles through the
     six seeded top-2 Zipf(1.2) routings (four empty experts on even steps).
-    `small`: the same layer shapes with two experts of 4096 routed rows each
-    (top-2 over two experts), about 3 GB on the device: the case a full ncu
-    capture of the grouped kernel runs on."""
+    `wk` = MOE_SMALL: the same layer shapes with two experts of 4096 routed
+    rows each (top-2 over two experts), about 3 GB on the device, the case a
+    full ncu capture of the grouped kernel runs on; MOE_DECAY: two experts
+    without tokens, the decay-only epilogue alone (2.8 GB of state read and
+    written, bound by HBM)."""
 
     peak_key = "bf16"
     opt = "AdamW"
 
-    def __init__(self, dev, state_dtype=torch.float32, small=False):
-        wk = wl.MOE_SMALL if small else wl.MOE
+    def __init__(self, dev, state_dtype=torch.float32, wk=None):
+        wk = wl.MOE if wk is None else wk
+        small = wk is not wl.MOE
         self.wk = wk
         E, N, M = wk.experts, wk.N, wk.M
         offs = []
@@ -474,7 +477,8 @@ WORKLOADS = {
     "attn_proj": lambda dev, st: AttnSet(dev, st),
     "linear": lambda dev, st: Dense(wl.LINEAR, dev, st),
     "moe": lambda dev, st: MoE(dev, st),
-    "moe_small": lambda dev, st: MoE(dev, st, small=True),
+    "moe_small": lambda dev, st: MoE(dev, st, wl.MOE_SMALL),
+    "moe_decay": lambda dev, st: MoE(dev, st, wl.MOE_DECAY),
     "fp8": lambda dev, st: Fp8(dev, st, "AdamW"),
     "fp8_sgdm": lambda dev, st: Fp8(dev, st, "SGD"),
     "fp8_quant": lambda dev, st: Fp8Quant(dev, st),
@@ -502,7 +506,7 @@ def oracle_case(workload):
     import oracle
     wk = {"mlp_down": wl.MLP_DOWN, "backward": wl.MLP_DOWN, "attn_proj": wl.ATTN_PROJ[0],
           "linear": wl.LINEAR, "fp8": wl.FP8, "fp8_sgdm": wl.FP8, "fp8_quant": wl.FP8,
-          "moe": wl.MOE, "moe_small": wl.MOE_SMALL}[workload]
+          "moe": wl.MOE, "moe_small": wl.MOE_SMALL, "moe_decay": wl.MOE_DECAY}[workload]
     K, N, M = wk.K // max(wk.experts, 1), wk.N, wk.M
     scales = (1.0, 1.0)
     if wk is wl.FP8:
@@ -903,10 +907,21 @@ def main():
     kernel_tf = job.flops / (ms * 1e-3) / 1e12
     t_tensor = job.flops / (peak_tf * 1e12)
     t_hbm = job.bytes / (bw * 1e9)
+    if t_tensor >= t_hbm:
+        roofline = {"bound": "tensor", "achieved": kernel_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                    "frac": kernel_tf / peak_tf, "peak_source": peak_note,
+                    # the same against the power-capped (seconds-long) cuBLAS rate
+                    "frac_sustained": kernel_tf / (peak_tf * sustained_ratio)}
+    else:
+        # bound by HBM: the algorithmic bytes of a step over its device time
+        gbs = job.bytes / (ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": bw, "unit": "GB/s",
+                    "frac": gbs / bw, "peak_source": f"hbm_gbs, {peak_src}"}
     prof = profile_summary() if (args.workload == "mlp_down" and args.state == "f32" and
                                  args.impl == "ours") else None
     traffic = prof.get("dram_bytes_per_launch") if prof else None
     gradw = prof.get("grad_w_hbm_bytes") if prof else None
+    roofline["traffic"] = traffic
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -920,11 +935,7 @@ def main():
         "pct_roofline": max(t_tensor, t_hbm) / (ms * 1e-3),
         "updates_per_s": job.params * world / (ms * 1e-3),
         "grad_w_hbm_bytes": gradw,
-        "roofline": {"bound": "tensor" if t_tensor >= t_hbm else "hbm", "achieved": kernel_tf,
-                     "peak": peak_tf, "unit": "TFLOP/s", "frac": kernel_tf / peak_tf,
-                     "peak_source": peak_note, "traffic": traffic,
-                     # the same against the power-capped (seconds-long) cuBLAS rate
-                     "frac_sustained": kernel_tf / (peak_tf * sustained_ratio)},
+        "roofline": roofline,
         "e2e": {"value": whole_job_rate(job.flops, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "pipelined": True,

@@ -174,5 +174,7 @@ MOE = Workload("moe E=8 tokens=16384 top2 d_in=14336 d_out=4096", K=32768, N=143
                steps=6, experts=8)
 MOE_SMALL = Workload("moe_small E=2 tokens=4096 top2 d_in=14336 d_out=4096", K=8192, N=14336,
                      M=4096, steps=1, experts=2)
+MOE_DECAY = Workload("moe_decay E=2 tokens=0 d_in=14336 d_out=4096", K=0, N=14336, M=4096,
+                     steps=1, experts=2)
 FP8 = Workload("fp8 K=32768 d_in=8192 d_out=8192", K=32768, N=8192, M=8192)
 FP8_SGD = SgdHP(lr=1e-2, momentum=0.9, wd=0.0)
