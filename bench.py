@@ -497,6 +497,12 @@ def oracle_sample(job_X, job_D, job_W, job_m, job_v, hp, step, rows, scales=(1.0
                  beta2=hp.beta2, eps=hp.eps, wd=hp.wd, step=step)
 
 
+# The contraction the CPU oracle times for each workload (see oracle_case).
+ORACLE_SPECS = {"mlp_down": wl.MLP_DOWN, "backward": wl.MLP_DOWN, "attn_proj": wl.ATTN_PROJ[0],
+                "linear": wl.LINEAR, "fp8": wl.FP8, "fp8_sgdm": wl.FP8, "fp8_quant": wl.FP8,
+                "moe": wl.MOE, "moe_small": wl.MOE_SMALL, "moe_decay": wl.MOE_DECAY}
+
+
 def oracle_case(workload):
     """The contraction the oracle times for a workload, on host copies of
     seeded inputs: the attention set by its widest projection, the MoE
@@ -504,9 +510,7 @@ def oracle_case(workload):
     with e4m3 inputs and their scales.  Returns (workload spec, X, dY,
     scales, K, N, M)."""
     import oracle
-    wk = {"mlp_down": wl.MLP_DOWN, "backward": wl.MLP_DOWN, "attn_proj": wl.ATTN_PROJ[0],
-          "linear": wl.LINEAR, "fp8": wl.FP8, "fp8_sgdm": wl.FP8, "fp8_quant": wl.FP8,
-          "moe": wl.MOE, "moe_small": wl.MOE_SMALL, "moe_decay": wl.MOE_DECAY}[workload]
+    wk = ORACLE_SPECS[workload]
     K, N, M = wk.K // max(wk.experts, 1), wk.N, wk.M
     scales = (1.0, 1.0)
     if wk is wl.FP8:

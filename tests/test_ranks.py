@@ -60,3 +60,10 @@ def test_one_rank_needs_no_process_group():
     b = load_bench()
     assert b.max_over_ranks(3.0, 1, None) == 3.0
     assert b.whole_job_rate(2e12, 1, 10.0) == pytest.approx(200.0)
+
+
+def test_every_workload_has_an_oracle_case():
+    """The reference arm and the CPU baseline time the oracle on a case of
+    each workload the bench offers."""
+    b = load_bench()
+    assert set(b.ORACLE_SPECS) == set(b.WORKLOADS)
