@@ -35,20 +35,25 @@
  * An nn.Linear weight [d_out, d_in] is the transpose of W; pass it as its
  * [d_in, d_out] row-major view.
  *
- * Ownership and ordering: every pointer is caller-owned device memory and
- * the library keeps no pointer after the call returns.  It allocates nothing
- * per call, with three exceptions: forge_quantize_e4m3 takes a few bytes of
- * scratch per call and forge_backward_adamw without a bf16 weight copy takes
- * one (see there), and an operand (X or dY) whose base is not
- * 16-byte aligned or whose row stride is not a multiple of 16 bytes is first
- * copied into a padded scratch buffer, allocated in stream order on `stream`
- * from a memory pool the library creates per device and freed in stream
- * order after the kernel (one extra read and write of that operand).  The
- * pool keeps the memory it has reserved for later calls (at most the largest
- * scratch in use at once) until the process ends.  If that allocation fails,
- * or the environment variable FORGE_MISALIGNED is "loader", the kernel
- * fetches such an operand itself with cp.async instead.  W, m, v, buf are
- * updated in place.  Calls are asynchronous and ordered on `stream`, and can
+ * Ownership and ordering: every pointer is caller-owned device memory of
+ * the current device (cudaMalloc, a memory pool or a virtual-memory mapping;
+ * host memory, managed memory and a peer GPU's memory are refused) and the
+ * library keeps no pointer after the call returns.  Calls whose operands TMA
+ * can address allocate nothing.  Two cases take stream-ordered scratch from
+ * a memory pool the library creates per device (allocated and freed on
+ * `stream`; the pool keeps what it has reserved, at most the largest scratch
+ * in use at once, until the process ends):
+ *   - an operand (X or dY) whose base is not 16-byte aligned or whose row
+ *     stride is not a multiple of 16 bytes (any odd bf16 width, any e4m3
+ *     width not divisible by 16) is first copied into rows padded to 16
+ *     bytes (one extra read and write of that operand).  If that allocation
+ *     fails, or the environment variable FORGE_MISALIGNED is "loader", an
+ *     operand whose rows are a multiple of 4 bytes is fetched by the kernel
+ *     itself with cp.async instead; other rows need the copy, and a failed
+ *     allocation returns FORGE_ERR_CUDA.  forge_wgrad_adamw_noalloc stages
+ *     into a fixed buffer instead;
+ *   - forge_backward_adamw without a bf16 weight copy (see there).
+ * W, m, v, buf are updated in place.  Calls are asynchronous and ordered on `stream`, and can
  * be captured in a CUDA graph once a first call has run on the device; the
  * return value reports only host-side validation
  * and launch errors.  Errors detected on the device (a bounded wait that
@@ -62,12 +67,14 @@
  *   - W's whole gradient for this step is X^T dY: no tied or shared use
  *     (the single-use guard of P1).
  *
- * Host-side checks run before any CUDA call, in this order: null pointers
+ * Host-side checks run before any launch, in this order: null pointers
  * (X and dY may be NULL only when K == 0), sizes (M >= 1, N >= 1, K >= 0,
  * E >= 1, step >= 1), dtypes, then the device (compute capability 10.3),
- * then alignment (X, dY: base and row stride multiples of 4 bytes, of 16
- * bytes to be read by TMA without staging; W, dW: 4-byte bases; m, v, buf:
- * bases aligned to their element size; see FORGE_ERR_MISALIGNED).
+ * then residency (every pointer the call reads or writes is device memory
+ * of the current device, else FORGE_ERR_INVALID_ARG), then alignment (X, dY:
+ * bases aligned to their element size, rows of any length; W, dW: 4-byte
+ * bases; m, v, buf: bases aligned to their element size; see
+ * FORGE_ERR_MISALIGNED).  The checks up to the dtypes need no GPU.
  */
 #ifndef FORGE_H
 #define FORGE_H
@@ -89,10 +96,12 @@ typedef struct CUstream_st* forge_stream_t;
 
 typedef enum {
     FORGE_OK = 0,
-    FORGE_ERR_INVALID_ARG = -1,       /* null pointer, bad size or hyperparameter */
+    FORGE_ERR_INVALID_ARG = -1,       /* null pointer, bad size or hyperparameter, or a
+                                         pointer that is not device memory of the
+                                         current device */
     FORGE_ERR_UNSUPPORTED_DTYPE = -2, /* dtype outside the supported set */
     FORGE_ERR_UNSUPPORTED_DEVICE = -3,/* no device, or compute capability != 10.3 */
-    FORGE_ERR_MISALIGNED = -4,        /* a base pointer or row stride the kernels cannot address */
+    FORGE_ERR_MISALIGNED = -4,        /* a base pointer not aligned to its element size */
     FORGE_ERR_CUDA = -5,              /* a CUDA runtime / driver call failed */
     FORGE_ERR_TIMEOUT = -6,           /* a device-side bounded wait ran out */
     FORGE_ERR_SCRATCH_TOO_SMALL = -7  /* forge_wgrad_adamw_noalloc: staging exceeds its buffer */
@@ -118,7 +127,8 @@ typedef enum {
  *   step         1-based step count after incrementing (as torch's AdamW).
  *   scales       device fp32 [2] = {sX, sdY} for FORGE_E4M3 inputs (the
  *                gradient is sX * sdY * X^T dY); must be NULL for bf16.
- * Row strides: N * elemsize(in_dtype) and M * elemsize(in_dtype) bytes.
+ * Row strides: N * elemsize(in_dtype) and M * elemsize(in_dtype) bytes, of
+ * any length (rows TMA cannot address are staged, see above).
  */
 FORGE_API forge_status forge_wgrad_adamw(const void* X, const void* dY, float* W, void* m, void* v,
                                int64_t M, int64_t N, int64_t K, forge_dtype in_dtype,
@@ -148,11 +158,18 @@ FORGE_API forge_status forge_wgrad_adamw(const void* X, const void* dY, float* W
  *     reads (the padding after each staged row lies outside the tensor maps),
  *     so nothing carries over from an earlier call.
  *   - First-call setup: the first call on a device resolves the buffer's
- *     address (cudaGetSymbolAddress), which loads the library module holding
- *     it and reserves its 256 MiB there for the life of the process.  Make
- *     that first call outside stream capture; later calls are capturable.
+ *     address (cudaGetSymbolAddress) and caches it for that device ordinal.
+ *     Under lazy module loading (the CUDA default) this first call loads the
+ *     library module holding the buffer and reserves its 256 MiB there for
+ *     the life of the process; with CUDA_MODULE_LOADING=EAGER every device
+ *     reserves it as soon as the process creates its context there, whether
+ *     or not this function is ever called.  Make that first call outside
+ *     stream capture; later calls are capturable.  The cached address
+ *     belongs to the device's primary context: calls after cudaDeviceReset,
+ *     or from another context on the device, are not supported.
  *   - FORGE_MISALIGNED=loader selects the kernel's own cp.async loader here
- *     too (no staging, no buffer).
+ *     too for rows that are a multiple of 4 bytes (no staging, no buffer);
+ *     other rows are still staged into the buffer.
  */
 FORGE_API forge_status forge_wgrad_adamw_noalloc(const void* X, const void* dY, float* W, void* m,
                                                  void* v, int64_t M, int64_t N, int64_t K,
@@ -181,8 +198,8 @@ FORGE_API forge_status forge_wgrad_adamw_noalloc(const void* X, const void* dY, 
  *   in_dtype     FORGE_BF16 only (else FORGE_ERR_UNSUPPORTED_DTYPE).
  *   state_dtype, lr, beta1, beta2, eps, wd, step: as forge_wgrad_adamw, the
  *                same for every problem.
- * Checks as forge_wgrad_adamw, per problem, before any launch; an operand
- * whose rows TMA cannot address is staged into the library's memory pool
+ * Checks as forge_wgrad_adamw, per problem, before any launch; operands
+ * whose rows TMA cannot address are staged into the library's memory pool
  * (one allocation per call), and a failed allocation returns FORGE_ERR_CUDA.
  */
 FORGE_API forge_status forge_wgrad_adamw_multi(const void* X, int64_t N, int64_t K, int32_t P,
@@ -204,12 +221,14 @@ FORGE_API forge_status forge_wgrad_adamw_multi(const void* X, int64_t N, int64_t
  *           or 1 when amax is 0 (n == 0 included).  NaN entries of x are left
  *           out of the amax (their codes are NaN).
  * Pass codes and scale as X (or dY) and scales[0] (or scales[1]) of an e4m3
- * call.  Two passes over x: the first writes one partial maximum per block
- * (at most four blocks per SM) into a scratch array from the library's memory
- * pool, allocated and freed in stream order on `stream`.  Errors: n < 0, scale NULL, or x / codes
+ * call.  Nothing is allocated: two passes over x, the first of which parks
+ * one partial maximum per block (at most four blocks per SM) in an aligned
+ * window of `codes`, which the second pass then overwrites with the codes.
+ * codes must not overlap x or scale.  Errors: n < 0, scale NULL, or x / codes
  * NULL with n > 0 -> FORGE_ERR_INVALID_ARG; x_dtype -> FORGE_ERR_UNSUPPORTED_DTYPE;
  * x not aligned to its element size or scale not 4-byte aligned ->
- * FORGE_ERR_MISALIGNED.
+ * FORGE_ERR_MISALIGNED; a pointer that is not device memory of the current
+ * device -> FORGE_ERR_INVALID_ARG.
  */
 FORGE_API forge_status forge_quantize_e4m3(const void* x, forge_dtype x_dtype, int64_t n,
                                            uint8_t* codes, float* scale, forge_stream_t stream);

@@ -18,6 +18,14 @@ Tolerances (the contract of the fused path):
 * W: |error| <= 1e-2 * lr wherever |g| > 1e-2 * rms(g) (per tensor; per
   expert in the grouped call; where an expert has g = 0 the mask is
   |m_exact| > 1e-2 * rms(m_exact)).
+* W on every element (diagnostic): W' recomputed in fp64 from the old W and
+  the kernel's own stored m', v' must match the kernel's W' within the
+  rounding of the epilogue's few fp32 operations and its approximate square
+  root and reciprocal (2^-19 of the update plus 2^-21 |W|); with bf16 state
+  the stored m', v' are the rounded copies of the values the update used,
+  so the update term gets 2^-7.  This covers the parameters whose gradient
+  is too small for the mask above, where the gradient's own fp32
+  accumulation error would dominate a comparison with the oracle.
 """
 import numpy as np
 
@@ -123,3 +131,27 @@ def check_grad_from_m(m_gpu, m_old, G, beta1, name="g from m"):
     assert e <= DW_TOL["bf16"], f"{name}: relative Frobenius {e:.3e} > {DW_TOL['bf16']}"
     assert e <= 1e-4, f"{name}: relative Frobenius {e:.3e} > diagnostic 1e-4"
     return e
+
+
+def check_W_from_state(gpu_W, W_old, m_new, v_new, hp, step, state_bf16, name="W (all)"):
+    """The diagnostic W bound over every element (module docstring).  m_new,
+    v_new: the kernel's stored state (fp32 values or bf16 bits)."""
+    dec = (lambda a: oracle.decode(np.asarray(a).astype(np.uint16))) if state_bf16 else \
+        (lambda a: np.asarray(a, np.float64))
+    m = dec(m_new).astype(np.float64).reshape(-1)
+    v = dec(v_new).astype(np.float64).reshape(-1)
+    W0 = np.asarray(W_old, np.float64).reshape(-1)
+    got = np.asarray(gpu_W, np.float64).reshape(-1)
+    lr, b1, b2, eps, wd = (float(hp.lr), float(hp.beta1), float(hp.beta2), float(hp.eps),
+                           float(hp.wd))
+    bc1 = 1.0 - b1 ** step
+    bc2 = 1.0 - b2 ** step
+    r = (m / bc1) / (np.sqrt(v / bc2) + eps)
+    want = W0 * (1.0 - lr * wd) - lr * r
+    upd = 2.0 ** -7 if state_bf16 else 2.0 ** -19
+    bound = upd * lr * np.abs(r) + 2.0 ** -21 * np.maximum(np.abs(W0), np.abs(want)) + 1e-38
+    err = np.abs(got - want)
+    bad = err > bound
+    assert not bad.any(), (f"{name}: {int(bad.sum())} of {err.size} elements off the update "
+                           f"their own state implies (worst {err.max():.3e})")
+    return float(err.max()) if err.size else 0.0

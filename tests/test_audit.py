@@ -3,9 +3,12 @@
 * No atomics anywhere in the CUDA sources: each output tile is owned by one
   CTA over the whole K, so nothing accumulates across CTAs (the pages'
   backward-contract audit forbids atomicAdd).
-* No multi-GPU multicast (multimem / NVLS), no Triton, no torch.compile on
-  the product path.  Multicast inside a CTA pair (an MMA commit signalling
-  both CTAs of a cluster on this GPU) is allowed.
+* No multi-GPU multicast (multimem / NVLS), no TMA multicast load
+  (cp.async.bulk ... .multicast::cluster): the library runs as one replica
+  per GPU, and every operand byte reaches shared memory through a plain load.
+  The one multicast form allowed is the MMA commit that signals both CTAs of
+  a pair (tcgen05.commit ... .multicast::cluster), an mbarrier arrive, not a
+  copy.  No Triton, no torch.compile on the product path.
 * The product path never imports the oracle, and the oracle never imports
   the product path.
 """
@@ -46,6 +49,28 @@ def test_no_multigpu_multicast_triton_or_compile():
         assert "multimem" not in code, f
         assert not re.search(r"^\s*(import|from)\s+triton", code, re.M), f
         assert "torch.compile" not in code, f
+
+
+def test_no_tma_multicast_loads():
+    """Every PTX string that names .multicast::cluster must be a tcgen05
+    commit, never a bulk copy."""
+    hits = []
+    for f in files(os.path.join(PKG, "csrc"), (".cu", ".cuh", ".h")):
+        code = strip_comments(open(f).read())
+        # join adjacent string literals so one instruction is one string
+        joined = re.sub(r'"\s*\n\s*"', "", code)
+        for lit in re.findall(r'"([^"\n]*)"', joined):
+            if "multicast" in lit and "tcgen05.commit" not in lit:
+                hits.append((os.path.basename(f), lit.strip()[:80]))
+            if re.search(r"cp\.async\.bulk[^;]*multicast", lit):
+                hits.append((os.path.basename(f), lit.strip()[:80]))
+    assert not hits, hits
+
+
+def test_kernel_form_choice_has_no_multicast_form():
+    api = open(os.path.join(PKG, "csrc", "forge_api.cu")).read()
+    assert '"quad"' not in api
+    assert "NPAIR" not in open(os.path.join(PKG, "csrc", "forge_kernel.cuh")).read()
 
 
 def test_product_and_oracle_are_separate():

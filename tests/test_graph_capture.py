@@ -51,3 +51,37 @@ def test_fused_step_replays_from_a_graph(cuda_device, M):
     assert fg.forge_get_device_status() == fg.FORGE_OK
     for a, b in ((We, Wg), (me, mg), (ve, vg)):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_no_alloc_staged_step_replays_from_a_graph(cuda_device):
+    """The no-allocation entry on its staging path (X rows of 1044 bytes, dY
+    rows of 8200): a first call outside capture sets the device up, then the
+    captured steps replay to the bits of the same calls made eagerly."""
+    dev = cuda_device
+    K, N, M = 4100, 522, 4100
+    X = wl.activations(K, N, wl.seed_of("gn-X"), device=dev)
+    D = wl.activations(K, M, wl.seed_of("gn-dY"), device=dev)
+    W, m, v = state(N, M, dev, 7)
+    We, me, ve = W.clone(), m.clone(), v.clone()
+    for step in (1, 2):
+        fg.forge_wgrad_adamw_noalloc(X, D, We, me, ve, step=step, **HP)
+    torch.cuda.synchronize()
+    Wg, mg, vg = W.clone(), m.clone(), v.clone()
+    fg.forge_wgrad_adamw_noalloc(X, D, Wg.clone(), mg.clone(), vg.clone(), step=1, **HP)
+    torch.cuda.synchronize()
+    graphs = []
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for step in (1, 2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                fg.forge_wgrad_adamw_noalloc(X, D, Wg, mg, vg, step=step, **HP)
+            graphs.append(g)
+    torch.cuda.synchronize()
+    assert torch.equal(Wg, W)
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    assert fg.forge_get_device_status() == fg.FORGE_OK
+    for a, b in ((We, Wg), (me, mg), (ve, vg)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))

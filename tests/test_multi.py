@@ -9,7 +9,8 @@ import torch
 
 import oracle
 import weight_grad_gemm_gb300 as fg
-from test_parity import HP, bf16_inputs, check_adamw, dev_state, host_state, warm_state
+from test_parity import (HP, adamw_ref, bf16_inputs, check_adamw, dev_state, host_state,
+                         warm_state)
 
 pytestmark = pytest.mark.gpu
 
@@ -54,7 +55,7 @@ def test_multi_matches_oracle(cuda_device, K, state_bf16):
     got = run_multi(cuda_device, X, Ds, states, step=3)
     for D, (W, m, v), g in zip(Ds, states, got):
         G = oracle.wgrad(X, D)
-        ref = oracle.adamw(G, W, m, v, step=3, **vars(HP))
+        ref = adamw_ref(G, W, m, v, step=3, **vars(HP))
         check_adamw(g, ref, G, HP.lr, state_bf16)
 
 
@@ -77,7 +78,7 @@ def test_multi_eight_problems_and_one(cuda_device):
     got = run_multi(cuda_device, X, Ds, states, step=2)
     for D, (W, m, v), g in zip(Ds, states, got):
         G = oracle.wgrad(X, D)
-        check_adamw(g, oracle.adamw(G, W, m, v, step=2, **vars(HP)), G, HP.lr, False)
+        check_adamw(g, adamw_ref(G, W, m, v, step=2, **vars(HP)), G, HP.lr, False)
     one = run_multi(cuda_device, X, Ds[4:5], states[4:5], step=2)
     assert all(np.array_equal(x, y) for x, y in zip(one[0], got[4]))
 
@@ -100,4 +101,16 @@ def test_multi_with_staged_x(cuda_device):
     got = run_multi(cuda_device, X, Ds, states, step=2)
     for D, (W, m, v), g in zip(Ds, states, got):
         G = oracle.wgrad(X, D)
-        check_adamw(g, oracle.adamw(G, W, m, v, step=2, **vars(HP)), G, HP.lr, False)
+        check_adamw(g, adamw_ref(G, W, m, v, step=2, **vars(HP)), G, HP.lr, False)
+
+
+def test_multi_odd_widths(cuda_device):
+    # d_in 263 (526-byte X rows) and d_out 301, 3 and 4097: every operand's
+    # rows are a multiple of 2 bytes only, staged by the byte-granular copy
+    K, N = 140, 263
+    Ms = [301, 3, 4097, 264]
+    X, Ds, states = case(K, N, Ms, 36, False)
+    got = run_multi(cuda_device, X, Ds, states, step=2)
+    for D, (W, m, v), g in zip(Ds, states, got):
+        G = oracle.wgrad(X, D)
+        check_adamw(g, adamw_ref(G, W, m, v, step=2, **vars(HP)), G, HP.lr, False)

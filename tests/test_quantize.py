@@ -1,6 +1,7 @@
 """GPU parity of the e4m3 amax quantiser against the oracle: codes and the
 scale must match bit for bit (the decision of each code is taken in fp32 on
-both sides: the quotient x / s, then the nearest e4m3 value, ties to even)."""
+both sides: the quotient x / s, then the nearest e4m3 value, ties to even),
+and nothing outside codes and scale is written."""
 import numpy as np
 import pytest
 import torch
@@ -55,6 +56,27 @@ def test_quantize_degenerate_and_misaligned(cuda_device):
     check(buf[1:])  # 4 bytes past a 16-byte boundary: the scalar path
     b16 = buf.to(torch.bfloat16)
     check(b16[3:])
+
+
+@pytest.mark.parametrize("n", [5, 7, 8, 9, 11, 12, 13, 2047, 2049, 70001])
+@pytest.mark.parametrize("offset", [0, 1, 2, 3])
+def test_quantize_codes_at_any_byte_offset(cuda_device, n, offset):
+    """The first pass parks its partial maxima in a 4-byte aligned window of
+    the codes buffer: codes that start 1-3 bytes past a word, and sizes
+    around the single-block threshold, must come out exactly as the oracle's
+    (the window is overwritten by the codes, never left behind)."""
+    dev = cuda_device
+    x = wl.with_outliers((n,), wl.seed_of("q-off", n, offset), device=dev)
+    buf = torch.full((n + 8,), 0xAB, dtype=torch.uint8, device=dev)
+    codes = buf[offset:offset + n]
+    scale = torch.full((1,), float("nan"), device=dev)
+    fg.forge_quantize_e4m3(x, codes, scale)
+    torch.cuda.synchronize()
+    want, ws = oracle.quantize_e4m3(x.cpu())
+    assert float(scale.item()) == ws
+    got = buf.cpu().numpy()
+    assert np.array_equal(got[offset:offset + n], want)
+    assert (got[:offset] == 0xAB).all() and (got[offset + n:] == 0xAB).all()
 
 
 def test_quantize_full_size_and_feeds_the_fp8_call(cuda_device):

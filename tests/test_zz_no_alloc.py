@@ -81,3 +81,43 @@ def test_no_alloc_refuses_staging_larger_than_its_buffer(cuda_device, monkeypatc
     fg.forge_wgrad_adamw(X, D, W, m, v, step=1, **HP)
     torch.cuda.synchronize()
     assert fg.forge_get_device_status() == fg.FORGE_OK
+
+
+# X rows of 1003 bf16 (2006 bytes) and dY rows of 1001 (2002 bytes) both
+# stage into 2016-byte rows: 4032 bytes per token row.  Either operand alone
+# fits the 256 MiB buffer at these row counts; only their sum decides.
+BOTH_N, BOTH_M = 1003, 1001
+ROWS_UNDER = (256 << 20) // 4032   # 66576 rows: 1024 bytes to spare
+ROWS_OVER = ROWS_UNDER + 1
+
+
+def test_no_alloc_refuses_when_both_staged_operands_together_overflow(cuda_device, monkeypatch):
+    monkeypatch.delenv("FORGE_MISALIGNED", raising=False)
+    dev = cuda_device
+    K = ROWS_OVER
+    X = torch.zeros((K, BOTH_N), dtype=torch.bfloat16, device=dev)
+    D = torch.zeros((K, BOTH_M), dtype=torch.bfloat16, device=dev)
+    W, m, v = state(BOTH_N, BOTH_M, 5, dev)
+    W0, m0, v0 = W.clone(), m.clone(), v.clone()
+    with pytest.raises(fg.ForgeError) as e:
+        fg.forge_wgrad_adamw_noalloc(X, D, W, m, v, step=1, **HP)
+    assert e.value.status == fg.FORGE_ERR_SCRATCH_TOO_SMALL
+    torch.cuda.synchronize()
+    for a, b in ((W, W0), (m, m0), (v, v0)):
+        assert torch.equal(a, b)
+
+
+def test_no_alloc_both_staged_operands_just_under_the_limit(cuda_device, monkeypatch):
+    monkeypatch.delenv("FORGE_MISALIGNED", raising=False)
+    dev = cuda_device
+    K = ROWS_UNDER
+    X = wl.activations(K, BOTH_N, wl.seed_of("na-X", "both"), device=dev)
+    D = wl.activations(K, BOTH_M, wl.seed_of("na-dY", "both"), device=dev)
+    W1, m1, v1 = state(BOTH_N, BOTH_M, 6, dev)
+    W2, m2, v2 = W1.clone(), m1.clone(), v1.clone()
+    fg.forge_wgrad_adamw(X, D, W1, m1, v1, step=2, **HP)
+    fg.forge_wgrad_adamw_noalloc(X, D, W2, m2, v2, step=2, **HP)
+    torch.cuda.synchronize()
+    assert fg.forge_get_device_status() == fg.FORGE_OK
+    for a, b in ((W1, W2), (m1, m2), (v1, v2)):
+        assert np.array_equal(bits(a), bits(b))

@@ -1,11 +1,12 @@
 // forge_api.cu -- the C ABI of libforge.so: argument validation, device
 // checks, TMA descriptor encoding, tile-grid sizing and kernel dispatch.
 //
-// Every check on the arguments runs before the first CUDA call, so invalid
-// calls fail with a status code even on a machine without a GPU.  The device
-// memory the library owns for the life of the process is the status word
-// below (once per device) and, once forge_wgrad_adamw_noalloc has run on a
-// device, its fixed staging buffer; the one per-call allocation is the
+// The checks on the arguments' values run before the first CUDA call, so
+// such calls fail with a status code even on a machine without a GPU; the
+// device, residency and alignment checks follow, all before any launch.  The
+// device memory the library owns for the life of the process is the status
+// word below (once per device) and, once forge_wgrad_adamw_noalloc has run on
+// a device, its fixed staging buffer; the one per-call allocation is the
 // staging copy of an operand whose rows TMA cannot address (stream-ordered,
 // from the library's memory pool, freed on the same stream after the kernel).
 #include <cuda.h>
@@ -37,6 +38,7 @@ __device__ int g_forge_status = 0;
 struct DeviceInfo {
     bool ready = false;
     bool supported = false;
+    int ordinal = -1;
     int sms = 0;
     int* status = nullptr;  // device address of g_forge_status on this device
 };
@@ -84,6 +86,7 @@ forge_status current_device(DeviceInfo** out)
             return FORGE_ERR_UNSUPPORTED_DEVICE;
         }
         d.supported = (major == 10 && minor == 3);
+        d.ordinal = dev;
         d.sms = sms;
         if (d.supported) {
             void* addr = nullptr;
@@ -163,6 +166,24 @@ __global__ void forge_wait_selftest_kernel(int64_t timeout_ns, int* status)
 
 forge_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FORGE_OK : FORGE_ERR_CUDA; }
 
+// Every pointer a call dereferences must be device memory (cudaMalloc, a
+// memory pool, a virtual-memory mapping) of the current device: TMA and the
+// epilogue address it directly, and host memory or a peer GPU's memory would
+// be reached over the wrong link or not at all.  Null entries are skipped.
+forge_status check_resident(int ordinal, const void* const* ptrs, int n)
+{
+    for (int i = 0; i < n; ++i) {
+        if (!ptrs[i]) continue;
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, ptrs[i]) != cudaSuccess) {
+            cudaGetLastError();
+            return FORGE_ERR_INVALID_ARG;
+        }
+        if (a.type != cudaMemoryTypeDevice || a.device != ordinal) return FORGE_ERR_INVALID_ARG;
+    }
+    return FORGE_OK;
+}
+
 // ------------------------------------------------------------------ operand staging
 
 // Copies `rows` rows of `units` U-sized units (source rows packed, `units`
@@ -193,14 +214,59 @@ __global__ void __launch_bounds__(256) forge_stage_rows_kernel(const U* __restri
     }
 }
 
-// Stages [rows, row_bytes] (base and stride aligned to `gran` = 8 or 4
-// bytes) into dst with a row stride of dst_row_bytes (a multiple of 16).
+// Rows whose base or length is not a multiple of 4 bytes (odd bf16 widths,
+// e4m3 widths not divisible by 4): each thread builds one 4-byte word of a
+// destination row from the one or two aligned source words that hold its
+// bytes (a funnel shift).  A source word is read only if it holds at least
+// one byte of the tensor, so no read leaves the memory pages the tensor
+// touches.  Bytes of the last word past the row's end land in the
+// destination row's padding, which the tensor map never reads.
+__global__ void __launch_bounds__(256) forge_stage_bytes_kernel(const uint8_t* __restrict__ src,
+                                                                uint32_t* __restrict__ dst,
+                                                                int64_t rows, int64_t row_bytes,
+                                                                int64_t dst_row_words)
+{
+    const int64_t words = (row_bytes + 3) / 4;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const uint8_t* s = src + r * row_bytes;
+        uint32_t* d = dst + r * dst_row_words;
+        for (int64_t w0 = threadIdx.x; w0 < words; w0 += 4 * blockDim.x) {
+            uint32_t v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t w = w0 + j * blockDim.x;
+                if (w >= words) continue;
+                const int64_t nv = row_bytes - 4 * w < 4 ? row_bytes - 4 * w : 4;
+                const uintptr_t first = reinterpret_cast<uintptr_t>(s + 4 * w);
+                const uintptr_t lo_word = first & ~static_cast<uintptr_t>(3);
+                const uintptr_t hi_word = (first + nv - 1) & ~static_cast<uintptr_t>(3);
+                const uint32_t* a = reinterpret_cast<const uint32_t*>(lo_word);
+                const uint32_t lo = __ldcs(a);
+                const uint32_t hi = hi_word != lo_word ? __ldcs(a + 1) : 0u;
+                v[j] = __funnelshift_r(lo, hi, static_cast<uint32_t>(8 * (first & 3)));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t w = w0 + j * blockDim.x;
+                if (w < words) d[w] = v[j];
+            }
+        }
+    }
+}
+
+// Stages [rows, row_bytes] (base and stride aligned to `gran` = 8, 4, 2 or 1
+// bytes) into dst (256-byte aligned) with a row stride of dst_row_bytes (a
+// multiple of 16).
 cudaError_t stage_rows(const void* src, void* dst, int64_t rows, int64_t row_bytes,
                        int64_t dst_row_bytes, int gran, int sms, cudaStream_t stream)
 {
     const int64_t blocks64 = rows < 8LL * sms ? rows : 8LL * sms;
     const int blocks = static_cast<int>(blocks64 > 0 ? blocks64 : 1);
-    if (gran == 8)
+    if (gran < 4)
+        forge_stage_bytes_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint8_t*>(src),
+                                                             static_cast<uint32_t*>(dst), rows,
+                                                             row_bytes, dst_row_bytes / 4);
+    else if (gran == 8)
         forge_stage_rows_kernel<uint2><<<blocks, 256, 0, stream>>>(
             static_cast<const uint2*>(src), static_cast<uint2*>(dst), rows, row_bytes / 8,
             dst_row_bytes / 8);
@@ -213,7 +279,9 @@ cudaError_t stage_rows(const void* src, void* dst, int64_t rows, int64_t row_byt
 
 // Operands whose rows TMA cannot address are either staged into a padded
 // copy (default) or fetched by the kernel's cp.async loader.
-// FORGE_MISALIGNED = loader | stage (read on every call) overrides.
+// FORGE_MISALIGNED = loader | stage (read on every call) overrides; rows
+// that are not a multiple of 4 bytes are staged either way (cp.async copies
+// 4, 8 or 16 bytes).
 bool stage_misaligned()
 {
     const char* e = std::getenv("FORGE_MISALIGNED");
@@ -250,17 +318,15 @@ cudaError_t dispatch_op(int op, int st, bool grouped, const Maps& m, const Param
 #undef FORGE_L
 }
 
-template <int IT, int NP>
+template <int IT>
 cudaError_t dispatch_pair(int op, int st, bool grouped, const Maps& m, const Params& p,
                           int64_t grid, cudaStream_t s)
 {
-#define FORGE_L(OPV, STV, G)                                                       \
-    launch_wgrad_pair<IT, OPV, STV, NP, G, false>(m.a, m.b, m.a1, m.b1, m.ak, m.bk, \
-                                                  kNoProblemMaps, p, grid, s)
-    if constexpr (NP == 1) {
-        if (grouped)
-            return st == ST_F32 ? FORGE_L(OP_ADAMW, ST_F32, true) : FORGE_L(OP_ADAMW, ST_BF16, true);
-    }
+#define FORGE_L(OPV, STV, G)                                                   \
+    launch_wgrad_pair<IT, OPV, STV, G, false>(m.a, m.b, m.a1, m.b1, m.ak, m.bk, \
+                                              kNoProblemMaps, p, grid, s)
+    if (grouped)
+        return st == ST_F32 ? FORGE_L(OP_ADAMW, ST_F32, true) : FORGE_L(OP_ADAMW, ST_BF16, true);
     switch (op) {
     case OP_ADAMW:
         return st == ST_F32 ? FORGE_L(OP_ADAMW, ST_F32, false) : FORGE_L(OP_ADAMW, ST_BF16, false);
@@ -273,19 +339,15 @@ cudaError_t dispatch_pair(int op, int st, bool grouped, const Maps& m, const Par
 }
 
 // Kernel form: 0 = one CTA per 128 x 256 tile; 1 = CTA pairs on 256 x 256
-// tiles; 2 = clusters of two pairs (512 x 256) sharing X through multicast.
-// Pairs serve calls whose operands TMA can address and whose d_out exceeds
-// 128, dense or grouped; the two-pair form (dense only) moves a quarter fewer
-// operand bytes through L2 but measured no faster on GB300, so it runs only
-// on request.  FORGE_KERNEL = single | pair | quad (read on every call)
-// overrides the automatic choice where that form applies.
-int kernel_form(const Params& p, bool grouped, bool manual)
+// tiles.  Pairs serve calls whose operands TMA can address and whose d_out
+// exceeds 128, dense or grouped.  FORGE_KERNEL = single | pair (read on every
+// call) overrides the automatic choice where that form applies.
+int kernel_form(const Params& p, bool manual)
 {
     if (manual) return 0;
     const char* e = std::getenv("FORGE_KERNEL");
     if (e && std::strcmp(e, "single") == 0) return 0;
     if (e && std::strcmp(e, "pair") == 0) return 1;
-    if (e && std::strcmp(e, "quad") == 0) return grouped ? 1 : 2;
     return p.M > BM ? 1 : 0;
 }
 
@@ -305,14 +367,17 @@ int32_t raster_band(int32_t tiles_m, int32_t default_band)
 }
 
 // How an operand [rows, ld] of elemsize es reaches shared memory: 0 = TMA
-// (16-byte aligned base and row stride), 8 or 4 = cp.async of that width
-// (base and row stride aligned to it), -1 = not addressable.
+// (16-byte aligned base and row stride), 8 or 4 = staged or fetched by
+// cp.async of that width (base and row stride aligned to it), 2 or 1 =
+// staged (base aligned to the element), -1 = a base not aligned to its
+// element size.
 int operand_path(const void* base, int64_t ld, int es)
 {
     const int64_t row = ld * es;
     if (aligned(base, 16) && row % 16 == 0) return 0;
     if (aligned(base, 8) && row % 8 == 0) return 8;
     if (aligned(base, 4) && row % 4 == 0) return 4;
+    if (aligned(base, static_cast<uintptr_t>(es))) return es;
     return -1;
 }
 
@@ -329,6 +394,11 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
     DeviceInfo* dev = nullptr;
     forge_status st = current_device(&dev);
     if (st != FORGE_OK) return st;
+    {
+        const void* ptrs[] = {rows > 0 ? X : nullptr, rows > 0 ? dY : nullptr, p.W, p.s1,
+                              p.s2, p.dW, p.scales, p.offsets};
+        if ((st = check_resident(dev->ordinal, ptrs, 8)) != FORGE_OK) return st;
+    }
 
     // the tile list of the smallest tiles must be indexable in 32 bits
     if (((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN) * p.E > INT32_MAX)
@@ -361,22 +431,26 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
 
     // Operands TMA cannot address: a padded staging copy with 16-byte rows
     // (one HBM-bound pass, then the TMA kernels), unless the caller asks for
-    // the in-kernel loader or the allocation fails.
+    // the in-kernel loader or the allocation fails; rows that are not a
+    // multiple of 4 bytes are always staged (the loader cannot copy them).
     const void* opA = dY;
     const void* opB = X;
     int64_t ldA = p.M * es, ldB = p.N * es;
     void* scratch = nullptr;  // pool allocation to return after the kernel
-    if (rows > 0 && (p.manual_a || p.manual_b) && stage_misaligned()) {
-        const int64_t pa = p.manual_a ? (ldA + 15) / 16 * 16 : 0;
-        const int64_t pb = p.manual_b ? (ldB + 15) / 16 * 16 : 0;
+    const bool want_stage = stage_misaligned();
+    const bool stage_a = rows > 0 && p.manual_a && (want_stage || p.gran_a < 4);
+    const bool stage_b = rows > 0 && p.manual_b && (want_stage || p.gran_b < 4);
+    const bool must_stage = (stage_a && p.gran_a < 4) || (stage_b && p.gran_b < 4);
+    if (stage_a || stage_b) {
+        const int64_t pa = stage_a ? (ldA + 15) / 16 * 16 : 0;
+        const int64_t pb = stage_b ? (ldB + 15) / 16 * 16 : 0;
         const int64_t need = (pa + pb) * rows;
         void* stage = nullptr;
         if (stage_from == StageFrom::Static) {
             // fixed buffer: refuse what does not fit, before any launch
             if (need > static_cast<int64_t>(static_stage_capacity()))
                 return FORGE_ERR_SCRATCH_TOO_SMALL;
-            int d = 0;
-            if (cudaGetDevice(&d) != cudaSuccess || static_stage_address(d, &stage) != cudaSuccess) {
+            if (static_stage_address(dev->ordinal, &stage) != cudaSuccess) {
                 cudaGetLastError();
                 return FORGE_ERR_CUDA;
             }
@@ -385,18 +459,19 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
         } else {
             cudaGetLastError();
             scratch = nullptr;
+            if (must_stage) return FORGE_ERR_CUDA;  // no loader fallback for such rows
         }
         if (stage) {
             uint8_t* sp = static_cast<uint8_t*>(stage);
             cudaError_t ce = cudaSuccess;
-            if (p.manual_a) {
+            if (stage_a) {
                 ce = stage_rows(dY, sp, rows, ldA, pa, p.gran_a, dev->sms, stream);
                 opA = sp;
                 ldA = pa;
                 p.manual_a = 0;
                 sp += pa * rows;
             }
-            if (ce == cudaSuccess && p.manual_b) {
+            if (ce == cudaSuccess && stage_b) {
                 ce = stage_rows(X, sp, rows, ldB, pb, p.gran_b, dev->sms, stream);
                 opB = sp;
                 ldB = pb;
@@ -410,16 +485,15 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
     }
 
     const bool man = p.manual_a || p.manual_b;
-    const int form = kernel_form(p, grouped, man);
+    const int form = kernel_form(p, man);
     Maps maps;
     std::memset(&maps, 0, sizeof maps);
     p.has_maps = rows > 0 ? 1 : 0;
     if (rows > 0) {
         st = FORGE_OK;
         if (!p.manual_a) st = encode_operand(&maps.a, opA, in_dtype, p.M, rows, ldA);
-        // two pairs fetch half of each X box's k rows apiece
         if (st == FORGE_OK && !p.manual_b)
-            st = encode_operand(&maps.b, opB, in_dtype, p.N, rows, ldB, form == 2 ? 2 : 1);
+            st = encode_operand(&maps.b, opB, in_dtype, p.N, rows, ldB);
         if (st == FORGE_OK && grouped && !p.manual_a)
             st = encode_operand(&maps.a1, opA, in_dtype, p.M, rows, ldA, 0);
         if (st == FORGE_OK && grouped && !p.manual_b)
@@ -434,7 +508,7 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
             return st;
         }
     }
-    const int64_t tile_m = form == 2 ? 4 * BM : (form == 1 ? 2 * BM : BM);
+    const int64_t tile_m = form == 1 ? 2 * BM : BM;
     const int64_t tiles_m = (p.M + tile_m - 1) / tile_m;
     const int64_t tiles_n = (p.N + BN - 1) / BN;
     const int64_t total = tiles_m * tiles_n * p.E;  // at least 1, within the bound checked above
@@ -446,16 +520,11 @@ forge_status run(const void* X, const void* dY, int64_t rows, forge_dtype in_dty
 
     const int ist = state_dtype == FORGE_BF16 ? ST_BF16 : ST_F32;
     cudaError_t e;
-    if (form > 0) {
+    if (form == 1) {
         // the launcher sizes the grid from the resident-cluster limit
-        if (form == 1)
-            e = in_dtype == FORGE_BF16
-                    ? dispatch_pair<IN_BF16, 1>(op, ist, grouped, maps, p, total, stream)
-                    : dispatch_pair<IN_E4M3, 1>(op, ist, grouped, maps, p, total, stream);
-        else
-            e = in_dtype == FORGE_BF16
-                    ? dispatch_pair<IN_BF16, 2>(op, ist, false, maps, p, total, stream)
-                    : dispatch_pair<IN_E4M3, 2>(op, ist, false, maps, p, total, stream);
+        e = in_dtype == FORGE_BF16
+                ? dispatch_pair<IN_BF16>(op, ist, grouped, maps, p, total, stream)
+                : dispatch_pair<IN_E4M3>(op, ist, grouped, maps, p, total, stream);
     } else {
         const int grid = static_cast<int>(total < dev->sms ? total : dev->sms);
         if (in_dtype == FORGE_BF16)
@@ -485,6 +554,16 @@ forge_status run_multi(const void* X, int64_t N, int64_t K, int32_t P, const voi
     DeviceInfo* dev = nullptr;
     forge_status st = current_device(&dev);
     if (st != FORGE_OK) return st;
+    {
+        const void* ptrs[1 + 4 * kMaxProblems] = {K > 0 ? X : nullptr};
+        for (int j = 0; j < P; ++j) {
+            ptrs[1 + 4 * j] = K > 0 ? dY[j] : nullptr;
+            ptrs[2 + 4 * j] = p.W_of[j];
+            ptrs[3 + 4 * j] = p.s1_of[j];
+            ptrs[4 + 4 * j] = p.s2_of[j];
+        }
+        if ((st = check_resident(dev->ordinal, ptrs, 1 + 4 * P)) != FORGE_OK) return st;
+    }
     constexpr int es = 2;  // bf16
     const int64_t tiles_n = (N + BN - 1) / BN;
     int64_t total = 0;
@@ -588,9 +667,9 @@ forge_status run_multi(const void* X, int64_t N, int64_t K, int32_t P, const voi
     p.status = dev->status;
     cudaError_t e =
         state_dtype == FORGE_BF16
-            ? launch_wgrad_pair<IN_BF16, OP_ADAMW, ST_BF16, 1, false, true>(
+            ? launch_wgrad_pair<IN_BF16, OP_ADAMW, ST_BF16, false, true>(
                   maps.a, maps.b, maps.a1, maps.b1, maps.ak, maps.bk, mm, p, total, stream)
-            : launch_wgrad_pair<IN_BF16, OP_ADAMW, ST_F32, 1, false, true>(
+            : launch_wgrad_pair<IN_BF16, OP_ADAMW, ST_F32, false, true>(
                   maps.a, maps.b, maps.a1, maps.b1, maps.ak, maps.bk, mm, p, total, stream);
     if (scratch) {
         const cudaError_t fe = scratch_free(scratch, stream);
@@ -648,6 +727,13 @@ forge_status forge::device_sms(int* sms)
     const forge_status st = current_device(&dev);
     if (st == FORGE_OK) *sms = dev->sms;
     return st;
+}
+
+forge_status forge::device_resident(const void* const* ptrs, int n)
+{
+    DeviceInfo* dev = nullptr;
+    const forge_status st = current_device(&dev);
+    return st == FORGE_OK ? check_resident(dev->ordinal, ptrs, n) : st;
 }
 
 namespace {

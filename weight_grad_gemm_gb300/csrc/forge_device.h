@@ -15,6 +15,11 @@ namespace forge {
 // on success *sms receives its SM count.
 forge_status device_sms(int* sms);
 
+// FORGE_OK when every non-null pointer of ptrs[0..n) is device memory of the
+// current device (checked with cudaPointerGetAttributes), else
+// FORGE_ERR_INVALID_ARG (or the device check's status).
+forge_status device_resident(const void* const* ptrs, int n);
+
 // Device address of the status word on the current device (after a
 // successful device_sms call).
 int* device_status_word();

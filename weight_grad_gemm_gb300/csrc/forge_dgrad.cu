@@ -566,6 +566,8 @@ extern "C" forge_status forge_dgrad(const void* dY, const void* Wb, void* dX, in
     int sms = 0;
     if ((st = device_sms(&sms)) != FORGE_OK) return st;
     if (K == 0) return FORGE_OK;
+    const void* ptrs[] = {dY, Wb, dX};
+    if ((st = device_resident(ptrs, 3)) != FORGE_OK) return st;
     return dgrad::launch(dY, Wb, dX, M, N, K, sms, reinterpret_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? FORGE_OK
@@ -589,6 +591,11 @@ extern "C" forge_status forge_backward_adamw(const void* X, const void* dY, floa
     const void* wb = Wb;
     int sms = 0;
     if ((st = device_sms(&sms)) != FORGE_OK) return st;
+    {
+        const void* ptrs[] = {K > 0 ? X : nullptr, K > 0 ? dY : nullptr, W, m, v,
+                              K > 0 ? Wb : nullptr, K > 0 ? dX : nullptr};
+        if ((st = device_resident(ptrs, 7)) != FORGE_OK) return st;
+    }
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     void* scratch = nullptr;
     if (K > 0) {

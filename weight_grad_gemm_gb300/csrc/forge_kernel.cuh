@@ -1062,21 +1062,15 @@ __global__ void __launch_bounds__(EpiFor<GROUPED>::threads, 1)
 // 256 fp32 result in its own TMEM.  A stage is therefore 32 KB per CTA
 // instead of 48 KB, so six stages fit where four did and each SM pulls a
 // third fewer operand bytes through L2 per MMA.  Each CTA runs the same
-// epilogue on its own 128 rows.
+// epilogue on its own 128 rows.  Every operand byte a CTA receives comes
+// from this GPU's memory through a plain (non-multicast) TMA load.
 //
-// With NPAIR = 2 a cluster holds two pairs stacked along d_out (a 512 x 256
-// tile) that need the same X columns: the CTA of each pair that holds B half
-// r fetches half of that half's k rows and multicasts them to its
-// counterpart in the other pair, so L2 delivers a quarter fewer bytes per SM.
-//
-// Synchronisation (per pair unless noted):
+// Synchronisation:
 //   full[s]   (even CTA)  its producer expects the 64 KB landing in the pair;
 //                         every load into the pair completes on it
-//   empty[s]  (each CTA)  every pair's MMA commit arrives in every CTA of the
-//                         cluster (a CTA's stage also receives the other
-//                         pair's multicast, so all pairs must be done with it)
+//   empty[s]  (each CTA)  the pair's MMA commit arrives in both CTAs
 //   tfull[b]  (each CTA)  the pair's MMA commit, when accumulator b is complete
-//   tempty[b] (even CTA)  all 16 epilogue warps of the pair arrive (the odd
+//   tempty[b] (even CTA)  all epilogue warps of the pair arrive (the odd
 //                         CTA's remotely) once accumulator b has been read
 constexpr int kPairStages = 6;
 constexpr int kPairStageA = 16384;  // this CTA's 128 rows of dY x BK
@@ -1085,10 +1079,10 @@ constexpr int kPairStageBytes = kPairStageA + kPairStageB;
 using SmemPair = SmemLayout<kPairStages * kPairStageBytes>;
 static_assert(SmemPair::alloc(kCarveoutExperts) + 1024 <= kCarveout196, "196 KB step");
 
-template <int IT, int OP, int ST, int NPAIR, bool GROUPED, bool MULTI>
-__global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUPED>::threads, 1)
+template <int IT, int OP, int ST, bool GROUPED, bool MULTI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiFor<GROUPED>::threads, 1)
     forge_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,   // dY
-                            const __grid_constant__ CUtensorMap tmB,   // X, boxes of BK / NPAIR rows
+                            const __grid_constant__ CUtensorMap tmB,   // X
                             const __grid_constant__ CUtensorMap tmA1,  // dY, one-row boxes (grouped)
                             const __grid_constant__ CUtensorMap tmB1,  // X, one-row boxes (grouped)
                             const __grid_constant__ CUtensorMap tmAk,  // dY, one-k-step boxes (grouped)
@@ -1096,9 +1090,7 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
                             const __grid_constant__ MultiMaps mm,      // dY of each problem (multi)
                             const __grid_constant__ Params p)
 {
-    static_assert(NPAIR == 1 || NPAIR == 2, "one or two pairs per cluster");
-    static_assert(!GROUPED || NPAIR == 1, "grouped calls use single pairs");
-    static_assert(!MULTI || (NPAIR == 1 && !GROUPED), "multi-problem calls: single pairs, dense");
+    static_assert(!MULTI || !GROUPED, "multi-problem calls are dense");
     static_assert(InTraits<IT>::BK == 4 * InTraits<IT>::umma_k,
                   "the one-k-step maps hold a quarter of a k-block");
     using TR = InTraits<IT>;
@@ -1127,20 +1119,14 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t crank = ptx::cluster_ctarank();
-    const uint32_t rank = crank & 1u;         // position in the pair
-    const uint32_t pair_id = crank >> 1;      // pair within the cluster
-    const uint32_t lead_rank = crank & ~1u;   // the pair's even CTA
-    const bool leader = rank == 0;
-    constexpr uint16_t kAllMask = static_cast<uint16_t>((1u << (2 * NPAIR)) - 1u);
-    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * pair_id));
-    // CTAs holding the same B half in every pair of the cluster
-    const uint16_t b_mask = static_cast<uint16_t>(NPAIR == 2 ? (0x5u << rank) : (1u << crank));
+    const uint32_t crank = ptx::cluster_ctarank();  // position in the pair
+    const bool leader = crank == 0;                 // the pair's even CTA
+    constexpr uint16_t kPairMask = 0x3;             // both CTAs of the pair
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPairStages; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], NPAIR);
+            ptx::mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&tfull[b], 1);
@@ -1172,14 +1158,14 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
     const uint32_t tmem_base = *tmem_slot;
 
     Sched sc;
-    sc.tiles_m = p.tiles_m;  // 256 * NPAIR-row tiles
+    sc.tiles_m = p.tiles_m;  // 256-row tiles
     sc.tiles_n = p.tiles_n;
-    sc.m_step = 2 * NPAIR * BM;
+    sc.m_step = 2 * BM;
     sc.m_off = static_cast<int32_t>(crank) * BM;
     sc.band = p.raster_band;
     sc.per_expert = p.tiles_m * p.tiles_n;
     sc.total = MULTI ? pick(p.tile_begin, p.P) : sc.per_expert * p.E;
-    sc.set_share(blockIdx.x / (2 * NPAIR), gridDim.x / (2 * NPAIR), GROUPED ? 1 : 0);
+    sc.set_share(blockIdx.x / 2, gridDim.x / 2, GROUPED ? 1 : 0);
     sc.offs = GROUPED ? s_offs : nullptr;
     sc.order = GROUPED ? s_order : nullptr;
     sc.multi = MULTI ? &p : nullptr;
@@ -1190,8 +1176,7 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
         // ---------------------------------------------------- TMA producer (both CTAs)
         if (lane == 0) {
             const uint64_t pol = ptx::policy_evict_last();
-            const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(&full[0]), lead_rank);
-            constexpr int kBRows = BK / NPAIR;  // k rows of each B box this CTA fetches
+            const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(&full[0]), 0);
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued_mask = 0, last_parity = 0;
@@ -1209,7 +1194,7 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
                     uint8_t* sb = sa + kPairStageA;
                     const uint32_t bar = full0 + s * 8;
                     const int32_t ky = static_cast<int32_t>(k);
-                    const int32_t nb = tl.n0 + static_cast<int32_t>(rank) * (BN / 2);
+                    const int32_t nb = tl.n0 + static_cast<int32_t>(crank) * (BN / 2);
                     if (GROUPED && tl.k_end - k < BK) {
                         // the expert's last k-block: rows past its end read as zeros
                         const int32_t kend = static_cast<int32_t>(tl.k_end);
@@ -1245,17 +1230,9 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
                             ptx::tma_load_2d_pair_hint(sa + i * kBoxBytes, mapA, bar,
                                                        tl.m0 + i * TR::box_mn, ky, pol);
 #pragma unroll
-                        for (int i = 0; i < kBBoxes; ++i) {
-                            if constexpr (NPAIR == 1) {
-                                ptx::tma_load_2d_pair(sb + i * kBoxBytes, &tmB, bar,
-                                                      nb + i * TR::box_mn, ky);
-                            } else {
-                                // rows [pair_id * kBRows, +kBRows) of this B box, to both pairs
-                                const int r0 = static_cast<int>(pair_id) * kBRows;
-                                ptx::tma_load_2d_pair_mc(sb + i * kBoxBytes + r0 * 128, &tmB, bar,
-                                                         nb + i * TR::box_mn, ky + r0, b_mask);
-                            }
-                        }
+                        for (int i = 0; i < kBBoxes; ++i)
+                            ptx::tma_load_2d_pair(sb + i * kBoxBytes, &tmB, bar,
+                                                  nb + i * TR::box_mn, ky);
                     }
                     issued_mask |= 1u << s;
                     last_parity = (last_parity & ~(1u << s)) | (ph << s);
@@ -1315,8 +1292,8 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
                             ptx::umma_f8_pair(d_tmem, ad, bd, kIdesc, first ? 0u : 1u);
                         first = 0;
                     }
-                    // stage s of every CTA that received this pair's loads is free
-                    ptx::umma_commit_pair(&empty[s], kAllMask);
+                    // stage s of both CTAs is free once these MMAs are done
+                    ptx::umma_commit_pair(&empty[s], kPairMask);
                     issued_any = true;
                     if (++s == kPairStages) {
                         s = 0;
@@ -1324,7 +1301,7 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
                     }
                 }
                 if (!ok) break;
-                ptx::umma_commit_pair(&tfull[b], pair_mask);  // both accumulators ready
+                ptx::umma_commit_pair(&tfull[b], kPairMask);  // both accumulators ready
                 ++ct;
             }
             if (!ok && issued_any) {
@@ -1337,7 +1314,7 @@ __global__ void __cluster_dims__(2 * NPAIR, 1, 1) __launch_bounds__(EpiFor<GROUP
             }
         }
     } else if (warp >= kEpiWarp0) {
-        const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), lead_rank);
+        const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), 0);
         epilogue_role<IT, OP, ST, EpiFor<GROUPED>, MULTI>(
             p, sc, tfull, tmem_base, abort_flag, warp, lane, [&](uint32_t b) {
                                       if (leader)

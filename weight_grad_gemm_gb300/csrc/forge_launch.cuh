@@ -17,9 +17,9 @@ cudaError_t launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmB, const C
                          const CUtensorMap& tmBk, const Params& p, int grid, cudaStream_t stream);
 
 // Same for the CTA-pair kernels.  The grid is sized from the number of
-// clusters of 2 * NPAIR CTAs that can be resident at once (a cluster must fit
-// in one GPC), never more than `total_tiles` clusters.
-template <int IT, int OP, int ST, int NPAIR, bool GROUPED, bool MULTI>
+// clusters of two CTAs that can be resident at once (a cluster must fit in
+// one GPC), never more than `total_tiles` clusters.
+template <int IT, int OP, int ST, bool GROUPED, bool MULTI>
 cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                               const CUtensorMap& tmA1, const CUtensorMap& tmB1,
                               const CUtensorMap& tmAk, const CUtensorMap& tmBk,
@@ -30,7 +30,7 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
 
 #define FORGE_DEFINE_LAUNCH_PAIR()                                                             \
     namespace forge {                                                                          \
-    template <int IT, int OP, int ST, int NPAIR, bool GROUPED, bool MULTI>                     \
+    template <int IT, int OP, int ST, bool GROUPED, bool MULTI>                                \
     cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,              \
                                   const CUtensorMap& tmA1, const CUtensorMap& tmB1,            \
                                   const CUtensorMap& tmAk, const CUtensorMap& tmBk,            \
@@ -41,14 +41,14 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
         int dev = 0;                                                                           \
         cudaError_t e = cudaGetDevice(&dev);                                                   \
         if (e != cudaSuccess) return e;                                                        \
-        auto kern = forge_wgrad_pair_kernel<IT, OP, ST, NPAIR, GROUPED, MULTI>;                \
+        auto kern = forge_wgrad_pair_kernel<IT, OP, ST, GROUPED, MULTI>;                       \
         int& mc = max_clusters[dev & 63];                                                      \
         if (__atomic_load_n(&mc, __ATOMIC_ACQUIRE) == 0) {                                     \
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
                                      SmemPair::alloc(kMaxExperts));                            \
             if (e != cudaSuccess) return e;                                                    \
             cudaLaunchConfig_t cfg = {};                                                       \
-            cfg.gridDim = dim3(2 * NPAIR, 1, 1);                                               \
+            cfg.gridDim = dim3(2, 1, 1);                                                       \
             cfg.blockDim = dim3(EpiFor<GROUPED>::threads, 1, 1);                               \
             cfg.dynamicSmemBytes = SmemPair::alloc(kMaxExperts);                               \
             int n = 0;                                                                         \
@@ -58,15 +58,15 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
             __atomic_store_n(&mc, n, __ATOMIC_RELEASE);                                        \
         }                                                                                      \
         const int64_t nc = total_tiles < mc ? total_tiles : mc;                                \
-        kern<<<static_cast<int>(2 * NPAIR * nc), EpiFor<GROUPED>::threads, SmemPair::alloc(p.E), \
+        kern<<<static_cast<int>(2 * nc), EpiFor<GROUPED>::threads, SmemPair::alloc(p.E),       \
                stream>>>(                                                                      \
             tmA, tmB, tmA1, tmB1, tmAk, tmBk, mm, p);                                          \
         return cudaGetLastError();                                                             \
     }                                                                                          \
     }
 
-#define FORGE_INSTANTIATE_PAIR(IT, OP, ST, NPAIR, G, MU)                                       \
-    template cudaError_t forge::launch_wgrad_pair<IT, OP, ST, NPAIR, G, MU>(                   \
+#define FORGE_INSTANTIATE_PAIR(IT, OP, ST, G, MU)                                              \
+    template cudaError_t forge::launch_wgrad_pair<IT, OP, ST, G, MU>(                          \
         const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,        \
         const CUtensorMap&, const CUtensorMap&, const forge::MultiMaps&,                       \
         const forge::Params&, int64_t, cudaStream_t);

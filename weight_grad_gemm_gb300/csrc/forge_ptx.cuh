@@ -346,20 +346,6 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorM
         : "memory");
 }
 
-// Multicast form: the box lands at the same offset in every CTA of
-// `cta_mask`, and each destination's byte count goes to the barrier at the
-// same offset in that destination's pair-leading (even) CTA.
-__device__ __forceinline__ void tma_load_2d_pair_mc(void* dst, const CUtensorMap* map,
-                                                    uint32_t bar_cluster_addr, int32_t x, int32_t y,
-                                                    uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr), "h"(cta_mask)
-        : "memory");
-}
-
 // Pair form of the four-row gather (completion counted on a barrier that may
 // live in the peer CTA).
 __device__ __forceinline__ void tma_gather4_2d_pair(void* dst, const CUtensorMap* map,

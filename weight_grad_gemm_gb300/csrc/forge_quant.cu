@@ -2,16 +2,20 @@
 // in front of an fp8 call: s = amax |x| / 448 (1 when amax is 0) and every
 // code is the e4m3 value nearest to x / s (ties to even).
 //
-// Two HBM-bound passes, because no code can be written before amax is known:
-// the first reduces |x| to one partial maximum per block (no atomics: the
-// partials go to a small stream-ordered scratch array from the library's
-// memory pool), the second has every
-// block fold the partials into amax, derive s exactly as the recipe does
-// (amax / 448 divided in fp32), and convert its share of x with the
-// hardware's round-to-nearest-even, saturating fp32 -> e4m3 conversion.
+// Two HBM-bound passes, because no code can be written before amax is known,
+// and no scratch memory: the first pass reduces |x| to one partial maximum
+// per block and parks the partials in the codes buffer itself (an aligned
+// window of it, which the codes overwrite later); one block folds them into
+// amax and writes s to the caller's scale; the second pass reads s and
+// converts every element with the hardware's round-to-nearest-even,
+// saturating fp32 -> e4m3 conversion.  Stream order keeps the three launches
+// apart, so no block overwrites a partial another block still needs.  No
+// atomics.  Inputs of fewer than 8 elements take one single-block launch
+// that does both passes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "forge.h"
@@ -100,19 +104,46 @@ __global__ void __launch_bounds__(kThreads) forge_amax_kernel(const T* __restric
     if (threadIdx.x == 0) part[blockIdx.x] = m;
 }
 
-template <typename T, bool VEC>
-__global__ void __launch_bounds__(kThreads) forge_quant_kernel(const T* __restrict__ x, int64_t n,
-                                                               const float* __restrict__ part,
-                                                               int nparts, uint8_t* __restrict__ q,
-                                                               float* __restrict__ scale)
+// s from amax, as the recipe divides it: in fp32, and 1 for an all-zero input
+__device__ __forceinline__ float scale_of(float amax)
+{
+    return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+}
+
+// One block: amax over the partials, then s into *scale.
+__global__ void __launch_bounds__(kThreads) forge_amax_fold_kernel(const float* __restrict__ part,
+                                                                   int nparts,
+                                                                   float* __restrict__ scale)
 {
     __shared__ float sh[32];
     float m = 0.0f;
     for (int i = threadIdx.x; i < nparts; i += blockDim.x) m = fmaxf(m, part[i]);
-    const float amax = block_max(m, sh);
-    const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-    if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
+    m = block_max(m, sh);
+    if (threadIdx.x == 0) *scale = scale_of(m);
+}
 
+// One block, both passes, for inputs too short to hold the partials.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) forge_quant_small_kernel(const T* __restrict__ x,
+                                                                     int64_t n,
+                                                                     uint8_t* __restrict__ q,
+                                                                     float* __restrict__ scale)
+{
+    __shared__ float sh[32];
+    float m = 0.0f;
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, fabsf(load1(x, i)));
+    const float s = scale_of(block_max(m, sh));
+    if (threadIdx.x == 0) *scale = s;
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x)
+        q[i] = static_cast<uint8_t>(e4m3x2(__fdiv_rn(load1(x, i), s), 0.0f) & 0xFFu);
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads) forge_quant_kernel(const T* __restrict__ x, int64_t n,
+                                                               uint8_t* __restrict__ q,
+                                                               const float* __restrict__ scale)
+{
+    const float s = *scale;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     int64_t i0 = 0;
@@ -144,38 +175,29 @@ template <typename T>
 cudaError_t quantize(const T* x, int64_t n, uint8_t* q, float* scale, int sms,
                      cudaStream_t stream)
 {
+    // partials window: the first 4-byte aligned byte of q onwards
+    const int64_t pad = static_cast<int64_t>((4 - reinterpret_cast<uintptr_t>(q) % 4) % 4);
+    if (n < pad + 4 * 2) {
+        forge_quant_small_kernel<T><<<1, kThreads, 0, stream>>>(x, n, q, scale);
+        return cudaGetLastError();
+    }
     const bool vec = aligned(x, 4 * sizeof(T)) && aligned(q, 4);
     const int64_t units = vec ? n / 4 + (n % 4) : n;
     int64_t want = (units + static_cast<int64_t>(kThreads) * kUnroll - 1) /
                    (static_cast<int64_t>(kThreads) * kUnroll);
-    const int64_t cap = static_cast<int64_t>(kBlocksPerSm) * sms;
+    const int64_t cap = std::min<int64_t>(static_cast<int64_t>(kBlocksPerSm) * sms, (n - pad) / 4);
     const int blocks = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
-    float* part = nullptr;
-    cudaError_t e = cudaSuccess;
-    const int nparts = n > 0 ? blocks : 0;
-    if (nparts > 0) {
-        e = forge::scratch_alloc(reinterpret_cast<void**>(&part), nparts * sizeof(float), stream);
-        if (e != cudaSuccess) return e;
-        if (vec)
-            forge_amax_kernel<T, true><<<blocks, kThreads, 0, stream>>>(x, n, part);
-        else
-            forge_amax_kernel<T, false><<<blocks, kThreads, 0, stream>>>(x, n, part);
-        e = cudaGetLastError();
-    }
-    if (e == cudaSuccess) {
-        if (vec)
-            forge_quant_kernel<T, true>
-                <<<blocks, kThreads, 0, stream>>>(x, n, part, nparts, q, scale);
-        else
-            forge_quant_kernel<T, false>
-                <<<blocks, kThreads, 0, stream>>>(x, n, part, nparts, q, scale);
-        e = cudaGetLastError();
-    }
-    if (part) {
-        const cudaError_t fe = forge::scratch_free(part, stream);
-        if (e == cudaSuccess) e = fe;
-    }
-    return e;
+    float* part = reinterpret_cast<float*>(q + pad);
+    if (vec)
+        forge_amax_kernel<T, true><<<blocks, kThreads, 0, stream>>>(x, n, part);
+    else
+        forge_amax_kernel<T, false><<<blocks, kThreads, 0, stream>>>(x, n, part);
+    forge_amax_fold_kernel<<<1, kThreads, 0, stream>>>(part, blocks, scale);
+    if (vec)
+        forge_quant_kernel<T, true><<<blocks, kThreads, 0, stream>>>(x, n, q, scale);
+    else
+        forge_quant_kernel<T, false><<<blocks, kThreads, 0, stream>>>(x, n, q, scale);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -188,8 +210,10 @@ extern "C" forge_status forge_quantize_e4m3(const void* x, forge_dtype x_dtype, 
     if (!aligned(scale, 4) || (x && !aligned(x, x_dtype == FORGE_F32 ? 4 : 2)))
         return FORGE_ERR_MISALIGNED;
     int sms = 0;
-    const forge_status st = forge::device_sms(&sms);
+    forge_status st = forge::device_sms(&sms);
     if (st != FORGE_OK) return st;
+    const void* ptrs[] = {n > 0 ? x : nullptr, n > 0 ? codes : nullptr, scale};
+    if ((st = forge::device_resident(ptrs, 3)) != FORGE_OK) return st;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const cudaError_t e =
         x_dtype == FORGE_F32

@@ -4,7 +4,11 @@
 // The buffer is a file-scope device array, so it lives in this translation
 // unit's own module: with lazy module loading (the CUDA default) its device
 // memory is reserved on a device only once the first no-allocation call
-// there resolves its address, and stays reserved for the life of the process.
+// there resolves its address, and stays reserved for the life of the process;
+// with CUDA_MODULE_LOADING=EAGER every context the process creates reserves
+// it at creation.  The address is cached per device ordinal and belongs to
+// that device's primary context: after cudaDeviceReset (or from another
+// context) the cached address is stale, so such calls are not supported.
 #include <cuda_runtime.h>
 
 #include <cstddef>
