@@ -808,6 +808,157 @@ def e2e_pipelined(job, ins_h, res_h, dev, stream, steps):
 
 # ---------------------------------------------------------------- our arm
 
+# ---------------------------------------------------------------- timing helpers
+
+def measure_e4m3_peak(dev, n=8192, reps=10):
+    """Dense e4m3 rate of this GPU in TFLOP/s: cuBLAS through torch._scaled_mm
+    on n^3 (fp32 accumulate, bf16 out, unit scales), best of `reps` launches
+    timed with CUDA events.  None if the call is unavailable."""
+    try:
+        a = torch.randn((n, n), device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), device=dev).to(torch.float8_e4m3fn).t()  # column-major
+        one = torch.ones((), device=dev)
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except (RuntimeError, TypeError, AttributeError):
+        return None
+
+
+def resident_bytes(job):
+    """Bytes of the device tensors a job keeps (inputs and state), each
+    storage counted once."""
+    seen, total = set(), 0
+    objs = [job] + list(getattr(job, "parts", []))
+    for o in objs:
+        for t in vars(o).values():
+            if isinstance(t, torch.Tensor) and t.is_cuda:
+                key = t.untyped_storage().data_ptr()
+                if key not in seen:
+                    seen.add(key)
+                    total += t.untyped_storage().nbytes()
+    return total
+
+
+def job_dtype(job):
+    return "e4m3" if getattr(job, "peak_key", "bf16") == "fp8" else "bf16"
+
+
+def l2_note(job):
+    return (f"flushed between steps (512 MiB write); inputs+state "
+            f"{resident_bytes(job) / 1e9:.2f} GB > 129 MB L2")
+
+
+def time_steps(job, steps, warmup, dev, local, flush, barrier):
+    """W untimed steps, then `steps` steps each bracketed by CUDA events on
+    the launch stream, L2 flushed before each (outside the events), clocks
+    sampled throughout.  Returns (per-step ms list, clock record, wall s)."""
+    import weight_grad_gemm_gb300 as fg
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        job.step()
+    torch.cuda.synchronize(dev)
+    if fg.forge_get_device_status() != fg.FORGE_OK:
+        raise RuntimeError("device status not OK after warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()  # evict L2 between steps (outside the timed events)
+        starts[i].record(stream)
+        job.step(stream=stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    wall = time.perf_counter() - wall0
+    time.sleep(0.2)
+    clk = clocks.stop()
+    if fg.forge_get_device_status() != fg.FORGE_OK:
+        raise RuntimeError("device status not OK after the timed region")
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], clk, wall
+
+
+def roofline_of(job, ms, peaks, peak_src, e4m3_peak):
+    """The roofline record of a job's step time: tensor-bound against the
+    peak of its own input type (bf16: the measured burst peak; e4m3: the
+    rate measured in this run, else the bf16 peak times the nominal fp8/bf16
+    ratio of 2), or HBM-bound against the measured copy bandwidth when its
+    algorithmic bytes take longer than its FLOP."""
+    peak_tf = peaks["bf16_tflops"]
+    peak_note = f"bf16_tflops burst, {peak_src}"
+    sustained_ratio = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) / peaks["bf16_tflops"]
+    if getattr(job, "peak_key", "bf16") == "fp8":
+        if e4m3_peak:
+            peak_tf = e4m3_peak
+            peak_note = "e4m3 dense, measured in this run (torch._scaled_mm 8192^3, best of 10)"
+        else:
+            peak_tf = peaks["bf16_tflops"] * 2.0
+            peak_note = f"bf16_tflops burst x 2 (nominal fp8/bf16), {peak_src}"
+    bw = peaks["hbm_gbs"]
+    kernel_tf = job.flops / (ms * 1e-3) / 1e12
+    t_tensor = job.flops / (peak_tf * 1e12)
+    t_hbm = job.bytes / (bw * 1e9)
+    if t_tensor >= t_hbm:
+        r = {"bound": "tensor", "achieved": kernel_tf, "peak": peak_tf, "unit": "TFLOP/s",
+             "frac": kernel_tf / peak_tf, "peak_source": peak_note,
+             # the same against the power-capped (seconds-long) cuBLAS rate
+             "frac_sustained": kernel_tf / (peak_tf * sustained_ratio)}
+    else:
+        gbs = job.bytes / (ms * 1e-3) / 1e9
+        r = {"bound": "hbm", "achieved": gbs, "peak": bw, "unit": "GB/s", "frac": gbs / bw,
+             "peak_source": f"hbm_gbs, {peak_src}"}
+    return r, max(t_tensor, t_hbm) / (ms * 1e-3)
+
+
+# The large configurations timed after the headline in the same process (the
+# headline is the MLP down-projection): (label, workload, state dtype, steps
+# rounded up to a multiple of this, so the MoE layer runs whole routing cycles).
+PER_CONFIG = [
+    ("attn_proj f32 state", "attn_proj", torch.float32, 1),
+    ("attn_proj bf16 state", "attn_proj", torch.bfloat16, 1),
+    ("moe f32 state, 6-step routing cycle", "moe", torch.float32, 6),
+    ("moe bf16 state, 6-step routing cycle", "moe", torch.bfloat16, 6),
+    ("fp8 e4m3 AdamW", "fp8", torch.float32, 1),
+    ("fp8 e4m3 SGD-momentum", "fp8_sgdm", torch.float32, 1),
+]
+
+
+def per_config_lines(args, dev, local, flush, barrier, world, peaks, peak_src, e4m3_peak):
+    out = {}
+    for label, name, st, cycle in PER_CONFIG:
+        job = WORKLOADS[name](dev, st)
+        steps = -(-args.steps // cycle) * cycle
+        per_ms, clk, wall = time_steps(job, steps, args.warmup, dev, local, flush, barrier)
+        ms = max_over_ranks(float(sum(per_ms)), world, dev) / steps
+        roof, pct = roofline_of(job, ms, peaks, peak_src, e4m3_peak)
+        out[label] = {
+            "workload": job.wk.name, "dtype": job_dtype(job),
+            "state": "f32" if st == torch.float32 else "bf16",
+            "steps": steps, "warmup": args.warmup, "ms_per_step": ms,
+            "value": whole_job_rate(job.flops, world, ms), "unit": UNIT,
+            "pct_roofline": pct, "roofline": roof,
+            "updates_per_s": job.params * world / (ms * 1e-3),
+            "gpu_launches": steps * getattr(job, "launches", 1),
+            "l2": l2_note(job), "clocks": clk, "wall_s_timed_region": wall}
+        del job
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -819,6 +970,10 @@ def main():
     ap.add_argument("--state", default="f32", choices=["f32", "bf16"],
                     help="optimizer state type (default fp32, the headline workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the chosen workload (by default the MLP down-projection "
+                         "line also times the attention set, the MoE layer and the fp8 "
+                         "workloads into its per_config object)")
     ap.add_argument("--ncu", metavar="DIR",
                     help="profile instead of timing: run the workload plainly, then under "
                          "ncu (launch list, then one full capture of the fused kernel), "
@@ -856,34 +1011,7 @@ def main():
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    for _ in range(args.warmup):
-        job.step()
-    torch.cuda.synchronize(dev)
-    if fg.forge_get_device_status() != fg.FORGE_OK:
-        raise RuntimeError("device status not OK after warm-up")
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    barrier()
-    torch.cuda.synchronize(dev)
-    wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()  # evict L2 between steps (outside the timed events)
-        starts[i].record(stream)
-        job.step(stream=stream)
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    wall = time.perf_counter() - wall0
-    time.sleep(0.2)
-    clk = clocks.stop()
-    if fg.forge_get_device_status() != fg.FORGE_OK:
-        raise RuntimeError("device status not OK after the timed region")
-
-    per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    per_step_ms, clk, wall = time_steps(job, args.steps, args.warmup, dev, local, flush, barrier)
     total_ms = max_over_ranks(float(sum(per_step_ms)), world, dev)
     ms = total_ms / args.steps
     value = whole_job_rate(job.flops, world, ms)
@@ -900,27 +1028,10 @@ def main():
     d2h = res_h.numel() * res_h.element_size()
 
     peaks, peak_src = load_peaks()
-    peak_tf = peaks["bf16_tflops"]
-    peak_note = f"bf16_tflops burst, {peak_src}"
-    if getattr(job, "peak_key", "bf16") == "fp8":
-        # e4m3 dense rate = the measured bf16 rate x the nominal fp8 / bf16 ratio (4.5 / 2.25)
-        peak_tf = peaks["bf16_tflops"] * 2.0
-        peak_note = f"bf16_tflops burst x 2 (nominal fp8/bf16), {peak_src}"
+    e4m3_peak = measure_e4m3_peak(dev) if args.impl == "ours" else None
+    roofline, pct = roofline_of(job, ms, peaks, peak_src, e4m3_peak)
+    peak_tf = roofline["peak"] if roofline["bound"] == "tensor" else peaks["bf16_tflops"]
     bw = peaks["hbm_gbs"]
-    sustained_ratio = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) / peaks["bf16_tflops"]
-    kernel_tf = job.flops / (ms * 1e-3) / 1e12
-    t_tensor = job.flops / (peak_tf * 1e12)
-    t_hbm = job.bytes / (bw * 1e9)
-    if t_tensor >= t_hbm:
-        roofline = {"bound": "tensor", "achieved": kernel_tf, "peak": peak_tf, "unit": "TFLOP/s",
-                    "frac": kernel_tf / peak_tf, "peak_source": peak_note,
-                    # the same against the power-capped (seconds-long) cuBLAS rate
-                    "frac_sustained": kernel_tf / (peak_tf * sustained_ratio)}
-    else:
-        # bound by HBM: the algorithmic bytes of a step over its device time
-        gbs = job.bytes / (ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": gbs, "peak": bw, "unit": "GB/s",
-                    "frac": gbs / bw, "peak_source": f"hbm_gbs, {peak_src}"}
     prof = profile_summary() if (args.workload == "mlp_down" and args.state == "f32" and
                                  args.impl == "ours") else None
     traffic = prof.get("dram_bytes_per_launch") if prof else None
@@ -931,12 +1042,13 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "impl": args.impl,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": job_dtype(job), "data": "synthetic",
         "config": {"workload": job.wk.name + f" {getattr(job, 'opt', 'AdamW')} {args.state} state",
                    "K": job.wk.K, "d_in": job.wk.N, "d_out": job.wk.M,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "flushed between steps (512 MiB write); inputs+state 1.0 GB > L2"},
-        "pct_roofline": max(t_tensor, t_hbm) / (ms * 1e-3),
+                   "l2": l2_note(job)},
+        "pct_roofline": pct,
+        "e4m3_peak_tflops": e4m3_peak,
         "updates_per_s": job.params * world / (ms * 1e-3),
         "grad_w_hbm_bytes": gradw,
         "roofline": roofline,
@@ -962,6 +1074,12 @@ def main():
                             "bytes": job.quant_bytes}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.impl == "ours":
         line["cpu_baseline"] = cpu_baseline(job, args.workload)
+    if args.workload == "mlp_down" and args.impl == "ours" and not args.no_per_config:
+        # the headline's own tensors are not needed any more
+        del job, ins_h, res_h
+        torch.cuda.empty_cache()
+        line["per_config"] = per_config_lines(args, dev, local, flush, barrier, world, peaks,
+                                              peak_src, e4m3_peak)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
