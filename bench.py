@@ -435,6 +435,74 @@ class Fp8Quant(Fp8):
         return float(np.median(q)), float(np.median(f))
 
 
+class OwnerStep(Dense):
+    """The data-parallel path with sharded optimizer state on the MLP
+    down-projection shapes: each step writes this rank's partial dW (fp32) with
+    forge_wgrad_only, sums the ranks' partials with a reduce-scatter (NCCL,
+    only when several ranks run; one rank owns every row), and applies the
+    owner's AdamW to its rows with forge_owner_adamw.  The gradient makes a
+    round trip through HBM here by construction (the collective needs it)."""
+
+    def __init__(self, dev, state_dtype=torch.float32):
+        super().__init__(wl.MLP_DOWN, dev, state_dtype)
+        from weight_grad_gemm_gb300 import owner
+        wk = self.wk
+        K, N, M = wk.K, wk.N, wk.M
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.ranges = owner.owner_ranges(N, self.world)
+        r0, r1 = self.ranges[self.rank]
+        self.shard = (r0, r1)
+        self.G = torch.empty((N, M), dtype=torch.float32, device=dev)
+        es = 4 if state_dtype == torch.float32 else 2
+        n_own = (r1 - r0) * M
+        # operands once, the partial gradient written once and read back by
+        # the collective or the owner, the owner's shard of W, m, v
+        self.owner_bytes = n_own * (4 + 8 + 4 * es)
+        self.bytes = (K * N + K * M) * 2 + N * M * 4 + self.owner_bytes
+        self.launches = 2
+        self.wk = wl.Workload(f"owner_mlp K={K} d_in={N} d_out={M} (partial dW, reduce-scatter "
+                              f"over {self.world} rank(s), owner AdamW)", K=K, N=N, M=M)
+
+    def step(self, X=None, D=None, stream=None):
+        import weight_grad_gemm_gb300 as fg
+        if not hasattr(self, "G"):  # the warm-up steps of the constructor
+            return Dense.step(self, X, D, stream)
+        from weight_grad_gemm_gb300 import owner
+        hp = self.hp
+        fg.forge_wgrad_only(self.X if X is None else X, self.D if D is None else D, self.G,
+                            stream=stream)
+        r0, r1 = self.shard
+        G = owner.reduce_scatter_rows(self.G, self.ranges) if self.world > 1 else self.G[r0:r1]
+        if r1 > r0:
+            fg.forge_owner_adamw(G, self.W[r0:r1], self.m[r0:r1], self.v[r0:r1], lr=hp.lr,
+                                 beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps, wd=hp.wd,
+                                 step=self.t, stream=stream)
+        self.t += 1
+
+    def parts_us(self, stream, flush, reps=5):
+        """Median device time of the partial dW and of the owner's step."""
+        import weight_grad_gemm_gb300 as fg
+        hp = self.hp
+        r0, r1 = self.shard
+        a, b = [], []
+        for _ in range(reps):
+            flush.zero_()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev[0].record(stream)
+            fg.forge_wgrad_only(self.X, self.D, self.G, stream=stream)
+            ev[1].record(stream)
+            fg.forge_owner_adamw(self.G[r0:r1], self.W[r0:r1], self.m[r0:r1], self.v[r0:r1],
+                                 lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps, wd=hp.wd,
+                                 step=self.t, stream=stream)
+            ev[2].record(stream)
+            ev[2].synchronize()
+            self.t += 1
+            a.append(ev[0].elapsed_time(ev[1]) * 1e3)
+            b.append(ev[1].elapsed_time(ev[2]) * 1e3)
+        return float(np.median(a)), float(np.median(b))
+
+
 class Unfused:
     """The unfused pair on the same inputs: cuBLAS bf16 matmul (fp32
     accumulate, rounded to bf16 on output), .float(), then PyTorch's fused
@@ -483,6 +551,7 @@ WORKLOADS = {
     "fp8_sgdm": lambda dev, st: Fp8(dev, st, "SGD"),
     "fp8_quant": lambda dev, st: Fp8Quant(dev, st),
     "backward": lambda dev, st: Backward(dev, st),
+    "owner_mlp": lambda dev, st: OwnerStep(dev, st),
 }
 
 
@@ -498,7 +567,8 @@ def oracle_sample(job_X, job_D, job_W, job_m, job_v, hp, step, rows, scales=(1.0
 
 
 # The contraction the CPU oracle times for each workload (see oracle_case).
-ORACLE_SPECS = {"mlp_down": wl.MLP_DOWN, "backward": wl.MLP_DOWN, "attn_proj": wl.ATTN_PROJ[0],
+ORACLE_SPECS = {"mlp_down": wl.MLP_DOWN, "backward": wl.MLP_DOWN, "owner_mlp": wl.MLP_DOWN,
+                "attn_proj": wl.ATTN_PROJ[0],
                 "linear": wl.LINEAR, "fp8": wl.FP8, "fp8_sgdm": wl.FP8, "fp8_quant": wl.FP8,
                 "moe": wl.MOE, "moe_small": wl.MOE_SMALL, "moe_decay": wl.MOE_DECAY}
 
@@ -1066,6 +1136,14 @@ def main():
         tf = 2.0 * wk.K * wk.N * wk.M / (d_us * 1e-6) / 1e12
         line["dgrad"] = {"us": d_us, "fused_us": f_us, "bound": "tensor", "achieved": tf,
                          "peak": peak_tf, "unit": "TFLOP/s", "frac": tf / peak_tf}
+    if isinstance(job, OwnerStep):
+        d_us, o_us = job.parts_us(stream, flush)
+        gbs = job.owner_bytes / (o_us * 1e-6) / 1e9
+        line["owner"] = {"wgrad_only_us": d_us, "owner_adamw_us": o_us, "bound": "hbm",
+                         "achieved": gbs, "peak": bw, "unit": "GB/s", "frac": gbs / bw,
+                         "bytes": job.owner_bytes,
+                         "collective": "reduce_scatter_tensor (NCCL)" if world > 1 else
+                         "none (one rank owns every row)"}
     if isinstance(job, Fp8Quant):
         q_us, f_us = job.parts_us(stream, flush)
         gbs = job.quant_bytes / (q_us * 1e-6) / 1e9

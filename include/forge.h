@@ -304,6 +304,40 @@ FORGE_API forge_status forge_grouped_wgrad_adamw(const void* X, const void* dY, 
                                        float eps, float wd, int64_t step, const float* scales,
                                        forge_stream_t stream);
 
+/*
+ * The owner's optimizer step behind a reduce-scatter (data parallelism with
+ * the optimizer state sharded, ZeRO-2 style; "Math verified, not asserted",
+ * P3: under a reduce-scatter every output tile has exactly one owner, which
+ * alone applies the update).  Each rank contracts its own tokens into a
+ * partial fp32 dW (forge_wgrad_only); a reduce-scatter sums the partials and
+ * hands every rank the rows of W it owns; the owner then calls this on its
+ * shard.  Unlike the fused calls this path reads a gradient from device
+ * memory: the partial gradients exist because the collective exchanges them.
+ *   G      device fp32 [n]: the summed gradient of the owner's shard.
+ *   W      device fp32 [n], updated in place.
+ *   m, v   device [n] of state_dtype (FORGE_F32 or FORGE_BF16), updated in place.
+ *   n      elements in the shard (a row range [r0, r1) of a row-major [N, M]
+ *          weight is the flat range [r0 M, r1 M)); n = 0 does nothing.
+ *   lr, beta1, beta2, eps, wd, step: as forge_wgrad_adamw.
+ * The update is the fused epilogue's arithmetic, operation for operation:
+ * given the dW that forge_wgrad_only computes for (X, dY), the result equals
+ * forge_wgrad_adamw's on (X, dY) bit for bit.  G must not overlap W, m, v.
+ * Errors: n < 0 or a NULL pointer with n > 0, or a hyperparameter out of
+ * range -> FORGE_ERR_INVALID_ARG; state_dtype -> FORGE_ERR_UNSUPPORTED_DTYPE;
+ * pointers outside device memory of the current device ->
+ * FORGE_ERR_INVALID_ARG; G, W not 4-byte aligned or m, v not aligned to
+ * their element size -> FORGE_ERR_MISALIGNED.  Allocates nothing.
+ */
+FORGE_API forge_status forge_owner_adamw(const float* G, float* W, void* m, void* v, int64_t n,
+                                         forge_dtype state_dtype, float lr, float beta1,
+                                         float beta2, float eps, float wd, int64_t step,
+                                         forge_stream_t stream);
+
+/* The same for SGD with momentum (mom as forge_wgrad_sgdm's). */
+FORGE_API forge_status forge_owner_sgdm(const float* G, float* W, void* mom, int64_t n,
+                                        forge_dtype state_dtype, float lr, float momentum,
+                                        float wd, forge_stream_t stream);
+
 /* Static description of a status code; never NULL. */
 FORGE_API const char* forge_status_string(forge_status status);
 

@@ -36,7 +36,8 @@ FORGE_F32 = 2
 EXPORTS = ("forge_wgrad_adamw", "forge_wgrad_adamw_noalloc", "forge_wgrad_adamw_multi",
            "forge_wgrad_sgdm", "forge_wgrad_only",
            "forge_quantize_e4m3", "forge_dgrad", "forge_backward_adamw",
-           "forge_grouped_wgrad_adamw", "forge_status_string", "forge_get_device_status",
+           "forge_grouped_wgrad_adamw", "forge_owner_adamw", "forge_owner_sgdm",
+           "forge_status_string", "forge_get_device_status",
            "forge_selftest_wait_timeout", "forge_version")
 
 
@@ -71,10 +72,13 @@ def lib() -> ctypes.CDLL:
     L.forge_wgrad_only.argtypes = [P, P, P, I64, I64, I64, I, P, P]
     L.forge_grouped_wgrad_adamw.argtypes = [P, P, P, P, P, P, I32, I64, I64, I64, I, I, F, F, F,
                                             F, F, I64, P, P]
+    L.forge_owner_adamw.argtypes = [P, P, P, P, I64, I, F, F, F, F, F, I64, P]
+    L.forge_owner_sgdm.argtypes = [P, P, P, I64, I, F, F, F, P]
     for f in ("forge_wgrad_adamw", "forge_wgrad_adamw_noalloc", "forge_wgrad_adamw_multi",
               "forge_wgrad_sgdm",
               "forge_wgrad_only", "forge_quantize_e4m3", "forge_dgrad", "forge_backward_adamw",
-              "forge_grouped_wgrad_adamw", "forge_get_device_status",
+              "forge_grouped_wgrad_adamw", "forge_owner_adamw", "forge_owner_sgdm",
+              "forge_get_device_status",
               "forge_selftest_wait_timeout"):
         getattr(L, f).restype = I
     L.forge_status_string.argtypes = [I]
@@ -275,6 +279,37 @@ def forge_grouped_wgrad_adamw(X, dY, W, m, v, offsets, *, lr, beta1, beta2, eps,
                                         _dtype_code(m), lr, beta1, beta2, eps, wd, int(step),
                                         _scales_ptr(scales, X), _stream(stream, W))
     _check(s, "forge_grouped_wgrad_adamw")
+
+
+def _same_numel(G, *ts):
+    for t in ts:
+        if t.numel() != G.numel():
+            raise ValueError(f"gradient shard and state must have one element each, got "
+                             f"{G.numel()} and {t.numel()}")
+
+
+def forge_owner_adamw(G, W, m, v, *, lr, beta1, beta2, eps, wd, step, stream=None):
+    """The owner's AdamW step on its shard: G (fp32, the reduce-scattered sum
+    of the ranks' partial dW), W (fp32), m, v (fp32 or bf16), all of one
+    shape, updated in place (see include/forge.h)."""
+    import torch
+    _same_numel(G, W, m, v)
+    if G.dtype != torch.float32 or W.dtype != torch.float32 or m.dtype != v.dtype:
+        raise TypeError("G and W must be float32, m and v one dtype")
+    s = lib().forge_owner_adamw(_ptr(G), _ptr(W), _ptr(m), _ptr(v), G.numel(), _dtype_code(m),
+                                lr, beta1, beta2, eps, wd, int(step), _stream(stream, W))
+    _check(s, "forge_owner_adamw")
+
+
+def forge_owner_sgdm(G, W, mom, *, lr, momentum, wd, stream=None):
+    """The owner's SGD-momentum step on its shard (see forge_owner_adamw)."""
+    import torch
+    _same_numel(G, W, mom)
+    if G.dtype != torch.float32 or W.dtype != torch.float32:
+        raise TypeError("G and W must be float32")
+    s = lib().forge_owner_sgdm(_ptr(G), _ptr(W), _ptr(mom), G.numel(), _dtype_code(mom), lr,
+                               momentum, wd, _stream(stream, W))
+    _check(s, "forge_owner_sgdm")
 
 
 def forge_status_string(status: int) -> str:

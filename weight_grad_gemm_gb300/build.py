@@ -23,7 +23,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libforge.so")
 
 SOURCES = ["forge_api.cu", "kernels_bf16.cu", "kernels_e4m3.cu", "kernels_pair_bf16.cu",
-           "kernels_pair_e4m3.cu", "forge_static_stage.cu", "forge_quant.cu", "forge_dgrad.cu"]
+           "kernels_pair_e4m3.cu", "forge_static_stage.cu", "forge_quant.cu", "forge_dgrad.cu",
+           "forge_owner.cu"]
 HEADERS = ["forge_ptx.cuh", "forge_kernel.cuh", "forge_launch.cuh", "forge_static_stage.h",
            "forge_device.h"]
 

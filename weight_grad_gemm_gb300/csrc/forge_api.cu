@@ -812,6 +812,33 @@ forge_status forge::adamw_checks(const void* X, const void* dY, const float* W, 
     return FORGE_OK;
 }
 
+namespace {
+
+// The owner-side step behind a reduce-scatter: checks, then one HBM-bound
+// elementwise launch over the shard (forge_owner.cu).
+forge_status run_owner(int op, const float* G, float* W, void* s1, void* s2, int64_t n,
+                       forge_dtype state_dtype, Params& p, cudaStream_t stream)
+{
+    DeviceInfo* dev = nullptr;
+    forge_status st = current_device(&dev);
+    if (st != FORGE_OK) return st;
+    if (n == 0) return FORGE_OK;
+    const void* ptrs[] = {G, W, s1, s2};
+    if ((st = check_resident(dev->ordinal, ptrs, 4)) != FORGE_OK) return st;
+    const uintptr_t sa = state_dtype == FORGE_BF16 ? 2 : 4;
+    const uintptr_t va = state_dtype == FORGE_BF16 ? 8 : 16;
+    if (!aligned(G, 4) || !aligned(W, 4) || !aligned(s1, sa) || (s2 && !aligned(s2, sa)))
+        return FORGE_ERR_MISALIGNED;
+    const bool vec = aligned(G, 16) && aligned(W, 16) && aligned(s1, va) && (!s2 || aligned(s2, va));
+    p.W = W;
+    p.s1 = s1;
+    p.s2 = s2;
+    return from_cuda(launch_owner(op, state_dtype == FORGE_BF16 ? ST_BF16 : ST_F32, G, p, n, vec,
+                                  dev->sms, stream));
+}
+
+}  // namespace
+
 extern "C" {
 
 forge_status forge_wgrad_adamw(const void* X, const void* dY, float* W, void* m, void* v,
@@ -967,6 +994,36 @@ forge_status forge_grouped_wgrad_adamw(const void* X, const void* dY, float* W, 
     fill_adam(p, lr, beta1, beta2, eps, wd, step);
     return run(X, dY, T_max, in_dtype, OP_ADAMW, state_dtype, true, p,
                reinterpret_cast<cudaStream_t>(stream));
+}
+
+forge_status forge_owner_adamw(const float* G, float* W, void* m, void* v, int64_t n,
+                               forge_dtype state_dtype, float lr, float beta1, float beta2,
+                               float eps, float wd, int64_t step, forge_stream_t stream)
+{
+    if (n < 0 || (n > 0 && (!G || !W || !m || !v))) return FORGE_ERR_INVALID_ARG;
+    if (state_dtype != FORGE_F32 && state_dtype != FORGE_BF16) return FORGE_ERR_UNSUPPORTED_DTYPE;
+    forge_status s;
+    if ((s = check_adam(lr, beta1, beta2, eps, wd, step)) != FORGE_OK) return s;
+    Params p{};
+    fill_adam(p, lr, beta1, beta2, eps, wd, step);
+    return run_owner(OP_ADAMW, G, W, m, v, n, state_dtype, p,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+forge_status forge_owner_sgdm(const float* G, float* W, void* mom, int64_t n,
+                              forge_dtype state_dtype, float lr, float momentum, float wd,
+                              forge_stream_t stream)
+{
+    if (n < 0 || (n > 0 && (!G || !W || !mom))) return FORGE_ERR_INVALID_ARG;
+    if (state_dtype != FORGE_F32 && state_dtype != FORGE_BF16) return FORGE_ERR_UNSUPPORTED_DTYPE;
+    if (!finite_nonneg(lr) || !finite_nonneg(momentum) || !finite_nonneg(wd))
+        return FORGE_ERR_INVALID_ARG;
+    Params p{};
+    p.lr = lr;
+    p.mu = momentum;
+    p.wd = wd;
+    return run_owner(OP_SGDM, G, W, mom, nullptr, n, state_dtype, p,
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* forge_status_string(forge_status status)

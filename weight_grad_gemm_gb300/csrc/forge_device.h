@@ -41,6 +41,15 @@ cudaError_t encode_bf16_kmajor(CUtensorMap* map, const void* base, int64_t inner
 cudaError_t scratch_alloc(void** ptr, size_t bytes, cudaStream_t stream);
 cudaError_t scratch_free(void* ptr, cudaStream_t stream);
 
+struct Params;
+
+// The owner-side optimizer step (forge_owner.cu): op OP_ADAMW or OP_SGDM,
+// st ST_F32 or ST_BF16, over n elements of the flat gradient G and the state
+// in p (W, s1, s2 and the step's coefficients); vec = every pointer aligned
+// for four-element vectors.
+cudaError_t launch_owner(int op, int st, const float* G, const Params& p, int64_t n, bool vec,
+                         int sms, cudaStream_t stream);
+
 // The host-side checks forge_wgrad_adamw makes before any launch, including
 // the alignment of X, W, m and v (dY is the caller's to check).
 forge_status adamw_checks(const void* X, const void* dY, const float* W, const void* m,
