@@ -716,6 +716,8 @@ def _csv_rows(path):
 # Workloads that hold too much device memory for a full (multi-pass) ncu
 # capture: their --ncu run stops after the one-pass launch list.
 FULL_CAPTURE_TOO_LARGE = {"moe"}
+# the kernel a workload's full capture targets, where it is not the fused one
+CAPTURE_KERNEL = {"owner_mlp": "forge_owner"}
 
 
 def run_ncu(args):
@@ -729,8 +731,8 @@ def run_ncu(args):
     out = os.path.abspath(args.ncu)
     os.makedirs(out, exist_ok=True)
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "2", "--warmup", "3",
-           "--no-cpu-baseline", "--e2e-steps", "1", "--workload", args.workload,
-           "--state", args.state]
+           "--no-cpu-baseline", "--no-per-config", "--e2e-steps", "1", "--workload",
+           args.workload, "--state", args.state]
     subprocess.run(cmd, check=True, stdout=subprocess.DEVNULL)
     launches = os.path.join(out, "launches.csv")
     subprocess.run(["ncu", "--metrics", "gpu__time_duration.sum", "--clock-control", "none",
@@ -749,8 +751,9 @@ def run_ncu(args):
     total = sum(t for _, t in per.values()) or 1.0
     table = [{"kernel": k, "launches": n, "total_us": t / 1e3, "share": t / total}
              for k, (n, t) in sorted(per.items(), key=lambda kv: -kv[1][1])]
-    # the first fused launch after the state-warming steps
-    kernel = "forge_wgrad"
+    # the first fused launch after the state-warming steps (the owner's step
+    # for the owner workload)
+    kernel = CAPTURE_KERNEL.get(args.workload, "forge_wgrad")
     # a full capture replays the launch about forty times, saving and
     # restoring device memory around each pass: only on workloads of a few GB
     # (the MoE layer has the two-expert `moe_small` case for it)
@@ -1098,7 +1101,10 @@ def main():
     d2h = res_h.numel() * res_h.element_size()
 
     peaks, peak_src = load_peaks()
-    e4m3_peak = measure_e4m3_peak(dev) if args.impl == "ours" else None
+    per_config = (args.workload == "mlp_down" and args.impl == "ours" and
+                  not args.no_per_config)
+    needs_e4m3 = per_config or getattr(job, "peak_key", "bf16") == "fp8"
+    e4m3_peak = measure_e4m3_peak(dev) if args.impl == "ours" and needs_e4m3 else None
     roofline, pct = roofline_of(job, ms, peaks, peak_src, e4m3_peak)
     peak_tf = roofline["peak"] if roofline["bound"] == "tensor" else peaks["bf16_tflops"]
     bw = peaks["hbm_gbs"]
@@ -1152,7 +1158,7 @@ def main():
                             "bytes": job.quant_bytes}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.impl == "ours":
         line["cpu_baseline"] = cpu_baseline(job, args.workload)
-    if args.workload == "mlp_down" and args.impl == "ours" and not args.no_per_config:
+    if per_config:
         # the headline's own tensors are not needed any more
         del job, ins_h, res_h
         torch.cuda.empty_cache()

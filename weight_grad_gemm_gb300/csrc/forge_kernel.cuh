@@ -97,6 +97,7 @@ struct SmemLayout {
     }
 };
 constexpr int kCarveout196 = 196 * 1024;
+constexpr int kSmemPerCtaMax = 227 * 1024;  // dynamic shared memory one CTA may take
 constexpr int kCarveoutExperts = 128;
 using SmemCta = SmemLayout<kStages * kStageBytes>;
 static_assert(SmemCta::alloc(kCarveoutExperts) + 1024 <= kCarveout196, "196 KB step");
@@ -1072,12 +1073,26 @@ __global__ void __launch_bounds__(EpiFor<GROUPED>::threads, 1)
 //   tfull[b]  (each CTA)  the pair's MMA commit, when accumulator b is complete
 //   tempty[b] (even CTA)  all epilogue warps of the pair arrive (the odd
 //                         CTA's remotely) once accumulator b has been read
-constexpr int kPairStages = 6;
 constexpr int kPairStageA = 16384;  // this CTA's 128 rows of dY x BK
 constexpr int kPairStageB = 16384;  // this CTA's 128 columns of X x BK
 constexpr int kPairStageBytes = kPairStageA + kPairStageB;
-using SmemPair = SmemLayout<kPairStages * kPairStageBytes>;
-static_assert(SmemPair::alloc(kCarveoutExperts) + 1024 <= kCarveout196, "196 KB step");
+#ifndef FORGE_GROUPED_PAIR_STAGES
+#define FORGE_GROUPED_PAIR_STAGES 6
+#endif
+// Operand stages per CTA: dense and multi-problem calls six (the 196 KB
+// carve-out step, a 60 KB L1); grouped calls FORGE_GROUPED_PAIR_STAGES
+// (compile time).  The ring and L1 share the SM's 256 KB: the ring covers the
+// operand loads' latency, L1 holds the epilogue's state loads in flight.
+template <bool GROUPED>
+struct PairRing {
+    static constexpr int stages = GROUPED ? FORGE_GROUPED_PAIR_STAGES : 6;
+    using Smem = SmemLayout<stages * kPairStageBytes>;
+};
+static_assert(PairRing<false>::Smem::alloc(kCarveoutExperts) + 1024 <= kCarveout196,
+              "196 KB step");
+static_assert(PairRing<true>::stages >= 4 &&
+                  PairRing<true>::Smem::alloc(8) + 1024 <= kSmemPerCtaMax,
+              "grouped ring and an eight-expert table within one CTA's shared memory");
 
 template <int IT, int OP, int ST, bool GROUPED, bool MULTI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiFor<GROUPED>::threads, 1)
@@ -1104,6 +1119,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiFor<GROUPED>::thr
     static_assert(kABoxes * kBoxBytes == kPairStageA && kBBoxes * kBoxBytes == kPairStageB,
                   "stage size");
 
+    constexpr int kPairStages = PairRing<GROUPED>::stages;
+    using SmemPair = typename PairRing<GROUPED>::Smem;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));

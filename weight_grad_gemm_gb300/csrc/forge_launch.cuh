@@ -43,14 +43,17 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
         if (e != cudaSuccess) return e;                                                        \
         auto kern = forge_wgrad_pair_kernel<IT, OP, ST, GROUPED, MULTI>;                       \
         int& mc = max_clusters[dev & 63];                                                      \
+        constexpr int kSmemMax = PairRing<GROUPED>::Smem::alloc(kMaxExperts) < kSmemPerCtaMax   \
+                                     ? PairRing<GROUPED>::Smem::alloc(kMaxExperts)             \
+                                     : kSmemPerCtaMax;                                         \
         if (__atomic_load_n(&mc, __ATOMIC_ACQUIRE) == 0) {                                     \
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
-                                     SmemPair::alloc(kMaxExperts));                            \
+                                     kSmemMax);                                                \
             if (e != cudaSuccess) return e;                                                    \
             cudaLaunchConfig_t cfg = {};                                                       \
             cfg.gridDim = dim3(2, 1, 1);                                                       \
             cfg.blockDim = dim3(EpiFor<GROUPED>::threads, 1, 1);                               \
-            cfg.dynamicSmemBytes = SmemPair::alloc(kMaxExperts);                               \
+            cfg.dynamicSmemBytes = kSmemMax;                                                   \
             int n = 0;                                                                         \
             e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);                                \
             if (e != cudaSuccess) return e;                                                    \
@@ -58,7 +61,9 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
             __atomic_store_n(&mc, n, __ATOMIC_RELEASE);                                        \
         }                                                                                      \
         const int64_t nc = total_tiles < mc ? total_tiles : mc;                                \
-        kern<<<static_cast<int>(2 * nc), EpiFor<GROUPED>::threads, SmemPair::alloc(p.E),       \
+        if (PairRing<GROUPED>::Smem::alloc(p.E) > kSmemMax) return cudaErrorInvalidValue;     \
+        kern<<<static_cast<int>(2 * nc), EpiFor<GROUPED>::threads,                             \
+               PairRing<GROUPED>::Smem::alloc(p.E),                                            \
                stream>>>(                                                                      \
             tmA, tmB, tmA1, tmB1, tmAk, tmBk, mm, p);                                          \
         return cudaGetLastError();                                                             \
