@@ -229,3 +229,34 @@ def test_owner_sgdm_bitwise_the_fused_call_and_edge_cases(cuda_device):
     assert L.forge_owner_adamw(host.ctypes.data, own[0].data_ptr(), own[1].data_ptr(),
                                own[1].data_ptr(), 16, fg.FORGE_F32, 1e-3, 0.9, 0.999, 1e-8, 0.0,
                                1, None) == fg.FORGE_ERR_INVALID_ARG
+
+
+@pytest.mark.gpu
+def test_owner_step_full_size_mlp_shapes_bitwise(cuda_device):
+    """The MLP down-projection shapes the owner workload benchmarks (K 8192,
+    d_in 14336, d_out 4096, warm fp32 state): owner(dW) equals the fused step
+    on every element, the shard split into two owners' row ranges."""
+    import torch
+
+    import weight_grad_gemm_gb300 as fg
+    import workloads as wl
+    dev = cuda_device
+    wk = wl.MLP_DOWN
+    K, N, M = wk.K, wk.N, wk.M
+    X = wl.activations(K, N, wl.seed_of("own-full", "X"), device=dev)
+    D = wl.activations(K, M, wl.seed_of("own-full", "dY"), device=dev)
+    W = wl.randn((N, M), wl.seed_of("own-full", "W"), device=dev, std=0.02)
+    m = wl.randn((N, M), wl.seed_of("own-full", "m"), device=dev, std=1e-3)
+    v = wl.randn((N, M), wl.seed_of("own-full", "v"), device=dev, std=1e-3) ** 2
+    hp = vars(wk.adam.f32())
+    fused = [t.clone() for t in (W, m, v)]
+    fg.forge_wgrad_adamw(X, D, *fused, step=4, **hp)
+    G = torch.empty((N, M), device=dev)
+    fg.forge_wgrad_only(X, D, G)
+    own = [t.clone() for t in (W, m, v)]
+    for r0, r1 in owner.owner_ranges(N, 2):
+        fg.forge_owner_adamw(G[r0:r1], *(t[r0:r1] for t in own), step=4, **hp)
+    torch.cuda.synchronize()
+    assert fg.forge_get_device_status() == fg.FORGE_OK
+    for a, b in zip(fused, own):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
