@@ -242,9 +242,13 @@ FORGE_API forge_status forge_quantize_e4m3(const void* x, forge_dtype x_dtype, i
  *   Wb  device [N, M] bf16: the weight as the forward pass used it (for a
  *       fp32 master W, its bf16 copy).
  *   dX  device [K, N] bf16, written.
- * in_dtype must be FORGE_BF16.  dY and Wb need 16-byte aligned bases and a
- * row stride (M * 2 bytes) that is a multiple of 16 (else
- * FORGE_ERR_MISALIGNED); K may be 0 (nothing is written).
+ * in_dtype must be FORGE_BF16; K may be 0 (nothing is written).  dY, Wb and
+ * dX need bases aligned to their element size (else FORGE_ERR_MISALIGNED);
+ * rows of any width are accepted: when dY's or Wb's base is not 16-byte
+ * aligned or M * 2 is not a multiple of 16, that operand is first copied into
+ * rows padded to 16 bytes in a stream-ordered scratch buffer from the
+ * library's memory pool (freed on `stream` after the launch; a failed
+ * allocation returns FORGE_ERR_CUDA).
  */
 FORGE_API forge_status forge_dgrad(const void* dY, const void* Wb, void* dX, int64_t M, int64_t N,
                                    int64_t K, forge_dtype in_dtype, forge_stream_t stream);
@@ -255,10 +259,11 @@ FORGE_API forge_status forge_dgrad(const void* dY, const void* Wb, void* dX, int
  * W, m, v (exactly forge_wgrad_adamw), both on `stream`, so dX always sees
  * the weights from before this step.  Wb is the bf16 copy of W the forward
  * pass used; with Wb == NULL the library first rounds W to bf16 (nearest
- * even) into a scratch copy (N * M * 2 bytes) from its memory pool, allocated
- * and freed in stream order on `stream`.  bf16 inputs only.  Every argument check of
- * both halves runs before the first launch; the arguments are those of
- * forge_dgrad and forge_wgrad_adamw.
+ * even) into a scratch copy (N rows of M * 2 bytes rounded up to 16) from its
+ * memory pool, allocated and freed in stream order on `stream`, together with
+ * any staging copy forge_dgrad would make.  bf16 inputs only.  Every argument
+ * check of both halves runs before the first launch; the arguments are those
+ * of forge_dgrad and forge_wgrad_adamw.
  */
 FORGE_API forge_status forge_backward_adamw(const void* X, const void* dY, float* W, void* m,
                                             void* v, const void* Wb, void* dX, int64_t M,

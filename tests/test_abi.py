@@ -160,8 +160,8 @@ def test_dgrad_and_backward_reject_invalid_arguments(L):
     assert d(M=0) == fg.FORGE_ERR_INVALID_ARG
     assert d(K=-1) == fg.FORGE_ERR_INVALID_ARG
     assert d(dt=fg.FORGE_E4M3) == fg.FORGE_ERR_UNSUPPORTED_DTYPE
-    assert d(M=60) == fg.FORGE_ERR_MISALIGNED          # 120-byte rows
-    assert d(Wb=ctypes.c_void_p(0x10008)) == fg.FORGE_ERR_MISALIGNED
+    assert d(Wb=ctypes.c_void_p(0x10001)) == fg.FORGE_ERR_MISALIGNED  # not bf16-aligned
+    assert d(dY=ctypes.c_void_p(0x10003)) == fg.FORGE_ERR_MISALIGNED
 
     def b(W=FAKE, Wb=FAKE, hp=HP, step=1, dt=fg.FORGE_BF16, st=fg.FORGE_F32):
         return L.forge_backward_adamw(FAKE, FAKE, W, FAKE, FAKE, Wb, FAKE, 64, 64, 64, dt, st,
@@ -172,6 +172,24 @@ def test_dgrad_and_backward_reject_invalid_arguments(L):
     assert b(dt=fg.FORGE_E4M3) == fg.FORGE_ERR_UNSUPPORTED_DTYPE
     assert b(st=fg.FORGE_E4M3) == fg.FORGE_ERR_UNSUPPORTED_DTYPE
     assert b(W=ctypes.c_void_p(0x10002)) == fg.FORGE_ERR_MISALIGNED
+
+
+def test_owner_steps_reject_invalid_arguments(L):
+    def o(G=FAKE, W=FAKE, m=FAKE, v=FAKE, n=64, st=fg.FORGE_F32, hp=HP, step=1):
+        return L.forge_owner_adamw(G, W, m, v, n, st, *hp, step, None)
+    assert o(n=-1) == fg.FORGE_ERR_INVALID_ARG
+    assert o(G=None) == fg.FORGE_ERR_INVALID_ARG
+    assert o(v=None) == fg.FORGE_ERR_INVALID_ARG
+    assert o(step=0) == fg.FORGE_ERR_INVALID_ARG
+    assert o(hp=(1e-3, 0.9, 1.0, 1e-8, 0.0)) == fg.FORGE_ERR_INVALID_ARG
+    assert o(st=fg.FORGE_E4M3) == fg.FORGE_ERR_UNSUPPORTED_DTYPE
+
+    def sg(G=FAKE, W=FAKE, mom=FAKE, n=64, st=fg.FORGE_F32, lr=1e-2, mu=0.9, wd=0.0):
+        return L.forge_owner_sgdm(G, W, mom, n, st, lr, mu, wd, None)
+    assert sg(mom=None) == fg.FORGE_ERR_INVALID_ARG
+    assert sg(lr=-1.0) == fg.FORGE_ERR_INVALID_ARG
+    assert sg(mu=float("nan")) == fg.FORGE_ERR_INVALID_ARG
+    assert sg(st=fg.FORGE_BF16 + 7) == fg.FORGE_ERR_UNSUPPORTED_DTYPE
 
 
 def test_selftest_rejects_bad_limit(L):
@@ -186,5 +204,9 @@ def test_valid_call_without_gpu_fails_closed(L):
     assert adamw(L, fn="forge_wgrad_adamw_noalloc") == fg.FORGE_ERR_UNSUPPORTED_DEVICE
     assert multi(L) == fg.FORGE_ERR_UNSUPPORTED_DEVICE
     assert L.forge_dgrad(FAKE, FAKE, FAKE, 64, 64, 64, fg.FORGE_BF16, None) == \
+        fg.FORGE_ERR_UNSUPPORTED_DEVICE
+    assert L.forge_dgrad(FAKE, FAKE, FAKE, 60, 64, 64, fg.FORGE_BF16, None) == \
+        fg.FORGE_ERR_UNSUPPORTED_DEVICE  # 120-byte rows are accepted (staged)
+    assert L.forge_owner_adamw(FAKE, FAKE, FAKE, FAKE, 64, fg.FORGE_F32, *HP, 1, None) == \
         fg.FORGE_ERR_UNSUPPORTED_DEVICE
     assert fg.forge_get_device_status() == fg.FORGE_ERR_UNSUPPORTED_DEVICE

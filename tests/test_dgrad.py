@@ -55,16 +55,67 @@ def test_dgrad_matches_oracle(cuda_device, dgrad_form, K, N, M):
     check_dx(dX, oracle.dgrad(oracle.as_bits(D.cpu()), oracle.as_bits(Wb.cpu())))
 
 
-def test_dgrad_no_tokens_and_misaligned_rows(cuda_device):
+def test_dgrad_no_tokens(cuda_device):
     dev = cuda_device
     D, Wb = inputs(0, 64, 64, 2, dev)
     dX = torch.empty((0, 64), dtype=torch.bfloat16, device=dev)
     fg.forge_dgrad(D, Wb, dX)
-    D, Wb = inputs(16, 64, 4100, 3, dev)  # 8200-byte rows: TMA cannot read them
-    dX = torch.empty((16, 64), dtype=torch.bfloat16, device=dev)
-    with pytest.raises(fg.ForgeError) as e:
-        fg.forge_dgrad(D, Wb, dX)
-    assert e.value.status == fg.FORGE_ERR_MISALIGNED
+    torch.cuda.synchronize()
+
+
+# d_out (the contraction here) of any width: rows of 8200, 602, 6 and 8194
+# bytes, which TMA cannot read, are staged into 16-byte rows first
+@pytest.mark.parametrize("K,N,M", [(160, 264, 4100), (130, 136, 301), (70, 300, 3),
+                                   (257, 520, 4097)])
+def test_dgrad_any_row_width(cuda_device, dgrad_form, K, N, M):
+    D, Wb = inputs(K, N, M, 3, cuda_device)
+    dX = torch.full((K, N), float("nan"), dtype=torch.bfloat16, device=cuda_device)
+    fg.forge_dgrad(D, Wb, dX)
+    torch.cuda.synchronize()
+    assert fg.forge_get_device_status() == fg.FORGE_OK
+    check_dx(dX, oracle.dgrad(oracle.as_bits(D.cpu()), oracle.as_bits(Wb.cpu())))
+
+
+def test_dgrad_offset_bases(cuda_device):
+    """dY and Wb starting 2 bytes into their allocations (aligned rows)."""
+    dev = cuda_device
+    K, N, M = 150, 264, 392
+    D, Wb = inputs(K, N, M, 4, dev)
+    db = torch.empty(K * M + 1, dtype=torch.bfloat16, device=dev)
+    wbb = torch.empty(N * M + 1, dtype=torch.bfloat16, device=dev)
+    Do, Wo = db[1:].view(K, M), wbb[1:].view(N, M)
+    Do.copy_(D)
+    Wo.copy_(Wb)
+    dX = torch.empty((K, N), dtype=torch.bfloat16, device=dev)
+    fg.forge_dgrad(Do, Wo, dX)
+    torch.cuda.synchronize()
+    check_dx(dX, oracle.dgrad(oracle.as_bits(D.cpu()), oracle.as_bits(Wb.cpu())))
+
+
+@pytest.mark.parametrize("given_copy", [True, False], ids=["Wb", "rounded"])
+def test_backward_odd_width(cuda_device, given_copy):
+    """The ordered step on d_out 301: dX from the staged (or freshly rounded,
+    padded) weight copy, then the fused update, equal bit for bit to the two
+    calls made separately."""
+    dev = cuda_device
+    K, N, M = 120, 264, 301
+    X = wl.activations(K, N, wl.seed_of("bw-odd", "X"), device=dev)
+    D = wl.activations(K, M, wl.seed_of("bw-odd", "dY"), device=dev)
+    W = wl.randn((N, M), wl.seed_of("bw-odd", "W"), device=dev, std=0.02)
+    m = torch.zeros_like(W)
+    v = torch.zeros_like(W)
+    Wb = W.to(torch.bfloat16)
+    W2, m2, v2 = W.clone(), m.clone(), v.clone()
+    dX = torch.empty((K, N), dtype=torch.bfloat16, device=dev)
+    dX2 = torch.empty_like(dX)
+    fg.forge_backward_adamw(X, D, W, m, v, dX, Wb=Wb if given_copy else None, step=1, **HP)
+    fg.forge_dgrad(D, Wb, dX2)
+    fg.forge_wgrad_adamw(X, D, W2, m2, v2, step=1, **HP)
+    torch.cuda.synchronize()
+    assert torch.equal(dX.view(torch.int16), dX2.view(torch.int16))
+    for a, b in ((W, W2), (m, m2), (v, v2)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    check_dx(dX, oracle.dgrad(oracle.as_bits(D.cpu()), oracle.as_bits(Wb.cpu())))
 
 
 def test_dgrad_full_size_sampled_rows(cuda_device, dgrad_form):

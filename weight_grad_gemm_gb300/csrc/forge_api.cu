@@ -781,11 +781,11 @@ int* forge::device_status_word()
 int64_t forge::wait_timeout() { return wait_timeout_ns(); }
 
 cudaError_t forge::encode_bf16_kmajor(CUtensorMap* map, const void* base, int64_t inner,
-                                      int64_t rows, uint32_t box_rows)
+                                      int64_t rows, uint32_t box_rows, int64_t ld_bytes)
 {
     if (!ensure_encode()) return cudaErrorNotSupported;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_bytes)};
     cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     const CUresult r =
@@ -793,6 +793,17 @@ cudaError_t forge::encode_bf16_kmajor(CUtensorMap* map, const void* base, int64_
                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t forge::stage_padded_rows(const void* src, void* dst, int64_t rows, int64_t row_bytes,
+                                     int64_t dst_row_bytes, cudaStream_t stream)
+{
+    DeviceInfo* dev = nullptr;
+    if (current_device(&dev) != FORGE_OK) return cudaErrorInvalidDevice;
+    const int gran = aligned(src, 8) && row_bytes % 8 == 0   ? 8
+                     : aligned(src, 4) && row_bytes % 4 == 0 ? 4
+                                                             : 1;
+    return stage_rows(src, dst, rows, row_bytes, dst_row_bytes, gran, dev->sms, stream);
 }
 
 forge_status forge::adamw_checks(const void* X, const void* dY, const float* W, const void* m,

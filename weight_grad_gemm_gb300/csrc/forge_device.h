@@ -27,11 +27,19 @@ int* device_status_word();
 // Bounded-wait limit in nanoseconds (FORGE_WAIT_TIMEOUT_MS, default 10 s).
 int64_t wait_timeout();
 
-// bf16 [rows, inner] row-major, 16-byte aligned base and row stride, read in
-// boxes of 64 elements of the inner (contraction) dimension x box_rows rows
-// with 128-byte swizzle: the K-major operand layout of tcgen05.mma.
+// bf16 [rows, inner] row-major, 16-byte aligned base and row stride ld_bytes
+// (a multiple of 16), read in boxes of 64 elements of the inner (contraction)
+// dimension x box_rows rows with 128-byte swizzle: the K-major operand layout
+// of tcgen05.mma.  Columns past `inner` read as zeros.
 cudaError_t encode_bf16_kmajor(CUtensorMap* map, const void* base, int64_t inner, int64_t rows,
-                               uint32_t box_rows);
+                               uint32_t box_rows, int64_t ld_bytes);
+
+// Copies [rows, row_bytes] from src (rows packed, base aligned to at least the
+// element size) into dst (256-byte aligned) with rows dst_row_bytes apart (a
+// multiple of 16 and >= row_bytes), on `stream`: the staging copy that makes
+// an operand TMA-addressable.  The padding after each row is left unwritten.
+cudaError_t stage_padded_rows(const void* src, void* dst, int64_t rows, int64_t row_bytes,
+                              int64_t dst_row_bytes, cudaStream_t stream);
 
 // Stream-ordered scratch from the library's own memory pool on the current
 // device (created on first use).  The pool keeps what it has reserved (its

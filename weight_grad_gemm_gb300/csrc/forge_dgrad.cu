@@ -453,16 +453,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 }
 
-// fp32 -> bf16, nearest even: the bf16 copy of W the input gradient reads
-// when the caller has none.
+// fp32 -> bf16, nearest even: the bf16 copy of W [rows, cols] the input
+// gradient reads when the caller has none, written with rows ld elements
+// apart (ld >= cols; the padding is left unwritten).
 __global__ void __launch_bounds__(256) forge_round_bf16_kernel(const float* __restrict__ src,
                                                                __nv_bfloat16* __restrict__ dst,
-                                                               int64_t n)
+                                                               int64_t rows, int64_t cols,
+                                                               int64_t ld)
 {
+    const int64_t n = rows * cols;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-         i += stride)
-        dst[i] = __float2bfloat16_rn(__ldcs(src + i));
+         i += stride) {
+        const int64_t r = ld == cols ? 0 : i / cols;
+        dst[i + r * (ld - cols)] = __float2bfloat16_rn(__ldcs(src + i));
+    }
 }
 
 bool aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
@@ -477,13 +482,21 @@ bool use_pairs(int64_t K)
     return K > BT;
 }
 
+// Row stride in bytes TMA needs for M bf16 columns: M * 2 rounded up to 16.
+int64_t padded_row(int64_t M) { return (M * 2 + 15) / 16 * 16; }
+
+// Whether a [*, M] bf16 operand at base must be staged before TMA reads it.
+bool needs_stage(const void* base, int64_t M) { return !aligned(base, 16) || (M * 2) % 16 != 0; }
+
+// ldA, ldB: the row strides in bytes of dY and Wb (multiples of 16, bases
+// 16-byte aligned).
 cudaError_t launch(const void* dY, const void* Wb, void* dX, int64_t M, int64_t N, int64_t K,
-                   int sms, cudaStream_t stream)
+                   int64_t ldA, int64_t ldB, int sms, cudaStream_t stream)
 {
     const bool pairs = use_pairs(K);
     CUtensorMap ta, tb;
-    if (encode_bf16_kmajor(&ta, dY, M, K, BT) != cudaSuccess ||
-        encode_bf16_kmajor(&tb, Wb, M, N, pairs ? BN / 2 : BN) != cudaSuccess)
+    if (encode_bf16_kmajor(&ta, dY, M, K, BT, ldA) != cudaSuccess ||
+        encode_bf16_kmajor(&tb, Wb, M, N, pairs ? BN / 2 : BN, ldB) != cudaSuccess)
         return cudaErrorInvalidValue;
     DParams p{};
     p.K = K;
@@ -545,11 +558,60 @@ forge_status check(const void* dY, const void* Wb, const void* dX, int64_t M, in
     if (K > 0 && (!dY || !dX)) return FORGE_ERR_INVALID_ARG;
     if (!Wb && !wb_optional) return FORGE_ERR_INVALID_ARG;
     if (in_dtype != FORGE_BF16) return FORGE_ERR_UNSUPPORTED_DTYPE;
-    // TMA reads dY and W rows: 16-byte aligned bases and row strides
-    if ((Wb && !aligned(Wb, 16)) || (dY && !aligned(dY, 16)) || (M * 2) % 16 != 0 ||
-        (dX && !aligned(dX, 2)))
+    // bases aligned to the element; rows TMA cannot address are staged
+    if ((Wb && !aligned(Wb, 2)) || (dY && !aligned(dY, 2)) || (dX && !aligned(dX, 2)))
         return FORGE_ERR_MISALIGNED;
     return FORGE_OK;
+}
+
+// dX = dY Wb^T with any row width: dY and Wb rows TMA cannot address (a base
+// or a row of M * 2 bytes not a multiple of 16) are staged into rows padded
+// to 16 bytes in one stream-ordered scratch allocation from the library's
+// pool, freed on `stream` after the launch.  With Wb == NULL the bf16 copy is
+// W (fp32 [N, M]) rounded to nearest even into that scratch.
+cudaError_t run(const void* dY, const void* Wb, const float* W, void* dX, int64_t M, int64_t N,
+                int64_t K, int sms, cudaStream_t stream)
+{
+    const int64_t pad = padded_row(M);
+    const bool stage_a = needs_stage(dY, M);
+    const bool stage_b = !Wb || needs_stage(Wb, M);
+    const int64_t bytes = (stage_a ? pad * K : 0) + (stage_b ? pad * N : 0);
+    void* scratch = nullptr;
+    if (bytes > 0) {
+        const cudaError_t e = scratch_alloc(&scratch, static_cast<size_t>(bytes), stream);
+        if (e != cudaSuccess) return e;
+    }
+    uint8_t* sp = static_cast<uint8_t*>(scratch);
+    const void* opA = dY;
+    const void* opB = Wb;
+    int64_t ldA = M * 2, ldB = M * 2;
+    cudaError_t e = cudaSuccess;
+    if (stage_a) {
+        e = stage_padded_rows(dY, sp, K, M * 2, pad, stream);
+        opA = sp;
+        ldA = pad;
+        sp += pad * K;
+    }
+    if (e == cudaSuccess && stage_b) {
+        if (!Wb) {
+            const int64_t n = N * M;
+            const int64_t want = (n + 255) / 256;
+            const int blocks = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);
+            forge_round_bf16_kernel<<<blocks, 256, 0, stream>>>(
+                W, reinterpret_cast<__nv_bfloat16*>(sp), N, M, pad / 2);
+            e = cudaGetLastError();
+        } else {
+            e = stage_padded_rows(Wb, sp, N, M * 2, pad, stream);
+        }
+        opB = sp;
+        ldB = pad;
+    }
+    if (e == cudaSuccess) e = launch(opA, opB, dX, M, N, K, ldA, ldB, sms, stream);
+    if (scratch) {
+        const cudaError_t fe = scratch_free(scratch, stream);
+        if (e == cudaSuccess) e = fe;
+    }
+    return e;
 }
 
 }  // namespace dgrad
@@ -568,10 +630,10 @@ extern "C" forge_status forge_dgrad(const void* dY, const void* Wb, void* dX, in
     if (K == 0) return FORGE_OK;
     const void* ptrs[] = {dY, Wb, dX};
     if ((st = device_resident(ptrs, 3)) != FORGE_OK) return st;
-    return dgrad::launch(dY, Wb, dX, M, N, K, sms, reinterpret_cast<cudaStream_t>(stream)) ==
-                   cudaSuccess
-               ? FORGE_OK
-               : FORGE_ERR_CUDA;
+    const cudaError_t e =
+        dgrad::run(dY, Wb, nullptr, dX, M, N, K, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) cudaGetLastError();
+    return e == cudaSuccess ? FORGE_OK : FORGE_ERR_CUDA;
 }
 
 extern "C" forge_status forge_backward_adamw(const void* X, const void* dY, float* W, void* m,
@@ -587,8 +649,6 @@ extern "C" forge_status forge_backward_adamw(const void* X, const void* dY, floa
     if ((st = adamw_checks(X, dY, W, m, v, M, N, K, in_dtype, state_dtype, lr, beta1, beta2, eps,
                            wd, step)) != FORGE_OK)
         return st;
-    // the weight copy the input gradient reads: the caller's, or W rounded now
-    const void* wb = Wb;
     int sms = 0;
     if ((st = device_sms(&sms)) != FORGE_OK) return st;
     {
@@ -596,29 +656,13 @@ extern "C" forge_status forge_backward_adamw(const void* X, const void* dY, floa
                               K > 0 ? Wb : nullptr, K > 0 ? dX : nullptr};
         if ((st = device_resident(ptrs, 7)) != FORGE_OK) return st;
     }
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    void* scratch = nullptr;
-    if (K > 0) {
-        if (!Wb) {
-            const int64_t n = N * M;
-            if (scratch_alloc(&scratch, static_cast<size_t>(n) * 2, s) != cudaSuccess) {
-                cudaGetLastError();
-                return FORGE_ERR_CUDA;
-            }
-            const int64_t want = (n + 255) / 256;
-            const int blocks = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);
-            dgrad::forge_round_bf16_kernel<<<blocks, 256, 0, s>>>(
-                W, static_cast<__nv_bfloat16*>(scratch), n);
-            wb = scratch;
-        }
-        // dX from the weights as they are before this step's update ...
-        cudaError_t e = cudaGetLastError();
-        if (e == cudaSuccess) e = dgrad::launch(dY, wb, dX, M, N, K, sms, s);
-        if (scratch) {
-            const cudaError_t fe = scratch_free(scratch, s);
-            if (e == cudaSuccess) e = fe;
-        }
-        if (e != cudaSuccess) return FORGE_ERR_CUDA;
+    // dX from the weights as they are before this step's update (the
+    // caller's bf16 copy, or W rounded now) ...
+    if (K > 0 &&
+        dgrad::run(dY, Wb, W, dX, M, N, K, sms, reinterpret_cast<cudaStream_t>(stream)) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return FORGE_ERR_CUDA;
     }
     // ... then the fused dW + AdamW that overwrites W, later on the same stream
     return forge_wgrad_adamw(X, dY, W, m, v, M, N, K, in_dtype, state_dtype, lr, beta1, beta2, eps,
