@@ -245,7 +245,7 @@ struct Sched {
             const int32_t rows_left = tm - g * bw;
             const int32_t gsz = rows_left < bw ? rows_left : bw;
             r.m0 = (g * bw + within % gsz) * m_step + m_off;
-            r.n0 = (within / gsz) * BN;
+            r.n0 = ((g & 1) ? tiles_n - 1 - within / gsz : within / gsz) * BN;
             r.k_begin = 0;
             r.k_end = K;
             r.pbase = 0;
@@ -255,8 +255,10 @@ struct Sched {
         int32_t j = t / per_expert;
         int32_t local = t - j * per_expert;
         // Raster: bands of `band` d_out tiles; within a band, d_out fastest,
-        // then across all d_in tiles.  A wave of tiles then touches only the
-        // band's dY columns, which stay in L2 while the band lasts.
+        // then across all d_in tiles, odd bands from the last d_in tile back
+        // to the first.  A wave of tiles then touches only the band's dY
+        // columns, which stay in L2 while the band lasts, and a band starts
+        // on the X columns the previous band ended on, still in L2.
         const int32_t per_band = band * tiles_n;
         const int32_t g = local / per_band;
         const int32_t within = local - g * per_band;
@@ -264,6 +266,7 @@ struct Sched {
         const int32_t gsz = rows_left < band ? rows_left : band;
         int32_t mt = g * band + within % gsz;
         int32_t nt = within / gsz;
+        if (g & 1) nt = tiles_n - 1 - nt;  // serpentine: odd bands walk d_in backwards
         r.m0 = mt * m_step + m_off;
         r.n0 = nt * BN;
         if (order) {
