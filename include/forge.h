@@ -58,7 +58,11 @@
  * return value reports only host-side validation
  * and launch errors.  Errors detected on the device (a bounded wait that
  * ran out) are recorded in a device status word read by
- * forge_get_device_status().
+ * forge_get_device_status().  The library resolves the device addresses of
+ * its own device variables (that status word, the no-allocation staging
+ * buffer) once per device ordinal and keeps them; they belong to the device's
+ * primary context, so calls after cudaDeviceReset, or from a context other
+ * than the primary one, are not supported.
  *
  * Caller preconditions (not checked):
  *   - X and dY do not overlap W, m, v, buf or dW.
