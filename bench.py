@@ -1013,23 +1013,40 @@ PER_CONFIG = [
 def per_config_lines(args, dev, local, flush, barrier, world, peaks, peak_src, e4m3_peak):
     out = {}
     for label, name, st, cycle in PER_CONFIG:
-        job = WORKLOADS[name](dev, st)
-        steps = -(-args.steps // cycle) * cycle
-        per_ms, clk, wall = time_steps(job, steps, args.warmup, dev, local, flush, barrier)
-        ms = max_over_ranks(float(sum(per_ms)), world, dev) / steps
-        roof, pct = roofline_of(job, ms, peaks, peak_src, e4m3_peak)
-        out[label] = {
-            "workload": job.wk.name, "dtype": job_dtype(job),
-            "state": "f32" if st == torch.float32 else "bf16",
-            "steps": steps, "warmup": args.warmup, "ms_per_step": ms,
-            "value": whole_job_rate(job.flops, world, ms), "unit": UNIT,
-            "pct_roofline": pct, "roofline": roof,
-            "updates_per_s": job.params * world / (ms * 1e-3),
-            "gpu_launches": steps * getattr(job, "launches", 1),
-            "l2": l2_note(job), "clocks": clk, "wall_s_timed_region": wall}
-        del job
+        try:
+            out[label] = per_config_line(args, dev, local, flush, barrier, world, peaks, peak_src,
+                                         e4m3_peak, name, st, cycle)
+        except Exception as exc:
+            # on one GPU a configuration's failure must not lose the headline
+            # line; with several ranks it must end every rank (the others
+            # would wait at the next barrier)
+            if world > 1:
+                raise
+            out[label] = {"error": f"{type(exc).__name__}: {exc}"[:300]}
         torch.cuda.empty_cache()
     return out
+
+
+def per_config_line(args, dev, local, flush, barrier, world, peaks, peak_src, e4m3_peak, name,
+                    st, cycle):
+    """One per-config entry: the workload set up, timed like the headline
+    (whole routing cycles for the MoE layer) and its roofline record."""
+    job = WORKLOADS[name](dev, st)
+    steps = -(-args.steps // cycle) * cycle
+    per_ms, clk, wall = time_steps(job, steps, args.warmup, dev, local, flush, barrier)
+    ms = max_over_ranks(float(sum(per_ms)), world, dev) / steps
+    roof, pct = roofline_of(job, ms, peaks, peak_src, e4m3_peak)
+    line = {
+        "workload": job.wk.name, "dtype": job_dtype(job),
+        "state": "f32" if st == torch.float32 else "bf16",
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms,
+        "value": whole_job_rate(job.flops, world, ms), "unit": UNIT,
+        "pct_roofline": pct, "roofline": roof,
+        "updates_per_s": job.params * world / (ms * 1e-3),
+        "gpu_launches": steps * getattr(job, "launches", 1),
+        "l2": l2_note(job), "clocks": clk, "wall_s_timed_region": wall}
+    del job
+    return line
 
 
 def main():
