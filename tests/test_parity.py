@@ -340,6 +340,18 @@ def test_grouped_many_experts(cuda_device, grouped_form):
     check_grouped(got, X, D, off, W, m, v, 4, sc, False)
 
 
+def test_grouped_max_experts(cuda_device, grouped_form):
+    """1024 experts, the most one call takes: the expert table fills shared
+    memory up to the next carve-out step; ragged counts of 0-5 tokens."""
+    rng = np.random.default_rng(26)
+    counts = rng.integers(0, 6, size=1024)
+    N, M = 8, 136
+    X, D, off, W, m, v, sc = grouped_case(list(counts), N, M, 27)
+    got = run_grouped(cuda_device, X, D, off, W, m, v, step=3)
+    assert fg.forge_get_device_status() == fg.FORGE_OK
+    check_grouped(got, X, D, off, W, m, v, 3, sc, False)
+
+
 def test_grouped_foreign_tokens_never_enter(cuda_device, grouped_form):
     """Expert e's gradient is the sum over its own tokens only: non-finite
     values in a neighbour's rows (which share the partial k-blocks at both
