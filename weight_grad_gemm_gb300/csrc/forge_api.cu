@@ -186,34 +186,6 @@ forge_status check_resident(int ordinal, const void* const* ptrs, int n)
 
 // ------------------------------------------------------------------ operand staging
 
-// Copies `rows` rows of `units` U-sized units (source rows packed, `units`
-// apart) into rows `dst_units` apart, leaving the padding at the end of each
-// destination row unwritten (the tensor map's extent stops before it).  A
-// block walks whole rows; each thread keeps four loads in flight.
-template <typename U>
-__global__ void __launch_bounds__(256) forge_stage_rows_kernel(const U* __restrict__ src,
-                                                               U* __restrict__ dst, int64_t rows,
-                                                               int64_t units, int64_t dst_units)
-{
-    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-        const U* s = src + r * units;
-        U* d = dst + r * dst_units;
-        for (int64_t u0 = threadIdx.x; u0 < units; u0 += 4 * blockDim.x) {
-            U v[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int64_t u = u0 + j * blockDim.x;
-                if (u < units) v[j] = __ldcs(s + u);
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int64_t u = u0 + j * blockDim.x;
-                if (u < units) d[u] = v[j];
-            }
-        }
-    }
-}
-
 // Rows whose base or length is not a multiple of 4 bytes (odd bf16 widths,
 // e4m3 widths not divisible by 4): each thread builds one 4-byte word of a
 // destination row from the one or two aligned source words that hold its
@@ -226,31 +198,75 @@ __global__ void __launch_bounds__(256) forge_stage_bytes_kernel(const uint8_t* _
                                                                 int64_t rows, int64_t row_bytes,
                                                                 int64_t dst_row_words)
 {
+    // flattened over the destination words of all rows, four in flight per
+    // thread: word i is word i % words of row i / words
     const int64_t words = (row_bytes + 3) / 4;
-    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-        const uint8_t* s = src + r * row_bytes;
-        uint32_t* d = dst + r * dst_row_words;
-        for (int64_t w0 = threadIdx.x; w0 < words; w0 += 4 * blockDim.x) {
-            uint32_t v[4];
+    const int64_t total = rows * words;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total;
+         i0 += 4 * stride) {
+        uint32_t v[4];
+        int64_t at[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int64_t w = w0 + j * blockDim.x;
-                if (w >= words) continue;
-                const int64_t nv = row_bytes - 4 * w < 4 ? row_bytes - 4 * w : 4;
-                const uintptr_t first = reinterpret_cast<uintptr_t>(s + 4 * w);
-                const uintptr_t lo_word = first & ~static_cast<uintptr_t>(3);
-                const uintptr_t hi_word = (first + nv - 1) & ~static_cast<uintptr_t>(3);
-                const uint32_t* a = reinterpret_cast<const uint32_t*>(lo_word);
-                const uint32_t lo = __ldcs(a);
-                const uint32_t hi = hi_word != lo_word ? __ldcs(a + 1) : 0u;
-                v[j] = __funnelshift_r(lo, hi, static_cast<uint32_t>(8 * (first & 3)));
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int64_t w = w0 + j * blockDim.x;
-                if (w < words) d[w] = v[j];
-            }
+        for (int j = 0; j < 4; ++j) {
+            const int64_t i = i0 + j * stride;
+            at[j] = -1;
+            if (i >= total) continue;
+            const int64_t r = i / words;
+            const int64_t w = i - r * words;
+            const int64_t nv = row_bytes - 4 * w < 4 ? row_bytes - 4 * w : 4;
+            const uintptr_t first = reinterpret_cast<uintptr_t>(src + r * row_bytes + 4 * w);
+            const uintptr_t lo_word = first & ~static_cast<uintptr_t>(3);
+            const uintptr_t hi_word = (first + nv - 1) & ~static_cast<uintptr_t>(3);
+            const uint32_t* a = reinterpret_cast<const uint32_t*>(lo_word);
+            const uint32_t lo = __ldcs(a);
+            const uint32_t hi = hi_word != lo_word ? __ldcs(a + 1) : 0u;
+            v[j] = __funnelshift_r(lo, hi, static_cast<uint32_t>(8 * (first & 3)));
+            at[j] = r * dst_row_words + w;
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (at[j] >= 0) dst[at[j]] = v[j];
+    }
+}
+
+// Rows of 8- or 4-byte granularity (base and length), flattened over the
+// destination's 16-byte chunks: thread i of the grid builds chunk i (row
+// i / chunks_per_row) from the 16 / sizeof(U) source units it covers and
+// stores it as one 16-byte vector, four chunks in flight per thread, so a
+// row boundary costs no extra memory round trip.  Units past a row's end
+// are not read; the chunk's bytes there land in the row's padding.
+template <typename U>
+__global__ void __launch_bounds__(256) forge_stage_chunks_kernel(const U* __restrict__ src,
+                                                                 uint4* __restrict__ dst,
+                                                                 int64_t rows, int64_t units,
+                                                                 int64_t dst_chunks)
+{
+    constexpr int kPer = 16 / sizeof(U);  // source units per destination chunk
+    const int64_t per_row = (units + kPer - 1) / kPer;
+    const int64_t total = rows * per_row;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total;
+         i0 += 4 * stride) {
+        uint4 v[4];
+        int64_t at[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t i = i0 + j * stride;
+            at[j] = -1;
+            if (i >= total) continue;
+            const int64_t r = i / per_row;
+            const int64_t c = i - r * per_row;
+            const U* sp = src + r * units + c * kPer;
+            U t[kPer];
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) t[k] = c * kPer + k < units ? __ldcs(sp + k) : U{};
+            v[j] = *reinterpret_cast<const uint4*>(t);
+            at[j] = r * dst_chunks + c;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (at[j] >= 0) dst[at[j]] = v[j];
     }
 }
 
@@ -260,20 +276,26 @@ __global__ void __launch_bounds__(256) forge_stage_bytes_kernel(const uint8_t* _
 cudaError_t stage_rows(const void* src, void* dst, int64_t rows, int64_t row_bytes,
                        int64_t dst_row_bytes, int gran, int sms, cudaStream_t stream)
 {
-    const int64_t blocks64 = rows < 8LL * sms ? rows : 8LL * sms;
-    const int blocks = static_cast<int>(blocks64 > 0 ? blocks64 : 1);
-    if (gran < 4)
-        forge_stage_bytes_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint8_t*>(src),
-                                                             static_cast<uint32_t*>(dst), rows,
-                                                             row_bytes, dst_row_bytes / 4);
-    else if (gran == 8)
-        forge_stage_rows_kernel<uint2><<<blocks, 256, 0, stream>>>(
-            static_cast<const uint2*>(src), static_cast<uint2*>(dst), rows, row_bytes / 8,
-            dst_row_bytes / 8);
-    else
-        forge_stage_rows_kernel<uint32_t><<<blocks, 256, 0, stream>>>(
-            static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), rows, row_bytes / 4,
-            dst_row_bytes / 4);
+    if (gran < 4) {
+        const int64_t words = rows * ((row_bytes + 3) / 4);
+        const int64_t want = (words + 4LL * 256 - 1) / (4LL * 256);
+        const int wblocks = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);
+        forge_stage_bytes_kernel<<<wblocks, 256, 0, stream>>>(static_cast<const uint8_t*>(src),
+                                                              static_cast<uint32_t*>(dst), rows,
+                                                              row_bytes, dst_row_bytes / 4);
+    } else {
+        const int64_t chunks = rows * ((row_bytes + 15) / 16);
+        const int64_t want = (chunks + 4LL * 256 - 1) / (4LL * 256);
+        const int cblocks = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);
+        if (gran == 8)
+            forge_stage_chunks_kernel<uint2><<<cblocks, 256, 0, stream>>>(
+                static_cast<const uint2*>(src), static_cast<uint4*>(dst), rows, row_bytes / 8,
+                dst_row_bytes / 16);
+        else
+            forge_stage_chunks_kernel<uint32_t><<<cblocks, 256, 0, stream>>>(
+                static_cast<const uint32_t*>(src), static_cast<uint4*>(dst), rows,
+                row_bytes / 4, dst_row_bytes / 16);
+    }
     return cudaGetLastError();
 }
 
