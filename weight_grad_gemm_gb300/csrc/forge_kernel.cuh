@@ -481,7 +481,42 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sched& sc,
     float gscale = 1.0f;
     if constexpr (IT == IN_E4M3) gscale = p.scales[0] * p.scales[1];
     uint32_t ct = 0;
-    for (int32_t it = 0; it < sc.count; ++it) {
+    // Two cursors over this CTA's share: the next tile with tokens (whose
+    // accumulators are read in the order the MMAs fill them) and the next
+    // decay-only tile (an expert without tokens: no accumulator).  With bf16
+    // state, while both remain, a warp streams a decay-only tile whenever the
+    // next accumulator is not ready yet, so the state of empty experts fills
+    // the time the epilogue would otherwise spend waiting on the MMAs (the
+    // MoE layer's routings with empty experts ran up to 7% faster).  With
+    // fp32 state the same policy was 12-15% slower on those routings: the
+    // extra state traffic beside the MMAs costs more than the idle time it
+    // fills, so fp32 state keeps the share's own order.  Which tile a warp
+    // takes changes only the timing: every tile's update is the same.
+    constexpr bool kFillWithDecay = ST == ST_BF16;
+    auto next_kind = [&](int32_t from, bool tokens) {
+        int32_t i = from;
+        for (; i < sc.count; ++i) {
+            const Tile x = sc.get(sc.nth(i));
+            if ((x.k_end > x.k_begin) == tokens) break;
+        }
+        return i;
+    };
+    int32_t it_tok = next_kind(0, true);
+    int32_t it_dec = next_kind(0, false);
+    while (it_tok < sc.count || it_dec < sc.count) {
+        bool take_tok = it_dec >= sc.count;
+        if (!kFillWithDecay && !take_tok && it_tok < sc.count) take_tok = it_tok < it_dec;
+        else if (!take_tok && it_tok < sc.count) {
+            int ready = 0;
+            if (lane == 0)
+                ready = ptx::mbar_test_wait(ptx::smem_addr(&tfull[ct & 1u]), (ct >> 1) & 1u) ? 1 : 0;
+            take_tok = __shfl_sync(0xffffffffu, ready, 0) != 0;
+        }
+        const int32_t it = take_tok ? it_tok : it_dec;
+        if (take_tok)
+            it_tok = next_kind(it_tok + 1, true);
+        else
+            it_dec = next_kind(it_dec + 1, false);
         const int32_t t = sc.nth(it);
         const Tile tl = sc.get(t);
         // the tile's d_out and state (per problem in a multi-problem call)
