@@ -506,10 +506,13 @@ class OwnerStep(Dense):
 class Unfused:
     """The unfused pair on the same inputs: cuBLAS bf16 matmul (fp32
     accumulate, rounded to bf16 on output), .float(), then PyTorch's fused
-    AdamW step -- the gradient makes a round trip through HBM."""
+    AdamW step -- the gradient makes a round trip through HBM.  With
+    fp32_out, cuBLAS writes the fp32 accumulator itself (no bf16 rounding,
+    torch.mm with out_dtype float32), then the same AdamW step."""
 
-    def __init__(self, job: Dense):
+    def __init__(self, job: Dense, fp32_out: bool = False):
         self.job = job
+        self.fp32_out = fp32_out
         self.W = torch.nn.Parameter(job.W.clone())
         hp = job.hp
         self.opt = torch.optim.AdamW([self.W], lr=hp.lr, betas=(hp.beta1, hp.beta2), eps=hp.eps,
@@ -526,8 +529,12 @@ class Unfused:
 
     def step(self, X=None, D=None, stream=None):
         j = self.job
-        g = torch.matmul((j.X if X is None else X).t(), j.D if D is None else D)
-        self.W.grad = g.float()
+        Xt = (j.X if X is None else X).t()
+        D = j.D if D is None else D
+        if self.fp32_out:
+            self.W.grad = torch.mm(Xt, D, out_dtype=torch.float32)
+        else:
+            self.W.grad = torch.matmul(Xt, D).float()
         self.opt.step()
 
     def inputs(self):
@@ -1054,7 +1061,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference", "unfused"])
+    ap.add_argument("--impl", default="ours",
+                    choices=["ours", "reference", "unfused", "unfused_f32"])
     ap.add_argument("--workload", default="mlp_down", choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--state", default="f32", choices=["f32", "bf16"],
@@ -1094,10 +1102,10 @@ def main():
     fg.lib()  # fails loudly if the CUDA library is not built
 
     job = WORKLOADS[args.workload](dev, torch.float32 if args.state == "f32" else torch.bfloat16)
-    if args.impl == "unfused":
+    if args.impl in ("unfused", "unfused_f32"):
         if not isinstance(job, Dense):
             ap.error("--impl unfused is defined for the dense workloads")
-        job = Unfused(job)
+        job = Unfused(job, fp32_out=args.impl == "unfused_f32")
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
