@@ -43,20 +43,21 @@
  * a memory pool the library creates per device (allocated and freed on
  * `stream`; the pool keeps what it has reserved, at most the largest scratch
  * in use at once, until the process ends):
- *   - an operand (X or dY) whose base is not 16-byte aligned or whose row
- *     stride is not a multiple of 16 bytes (any odd bf16 width, any e4m3
- *     width not divisible by 16) is first copied into rows padded to 16
- *     bytes (one extra read and write of that operand).  If that allocation
- *     fails, or the environment variable FORGE_MISALIGNED is "loader", an
- *     operand whose rows are a multiple of 4 bytes is fetched by the kernel
- *     itself with cp.async instead; other rows need the copy, and a failed
+ *   - an operand (X or dY; for dX, dY or Wb) whose base is not 16-byte
+ *     aligned or whose row stride is not a multiple of 16 bytes (any odd
+ *     bf16 width, any e4m3 width not divisible by 16) is first copied into
+ *     rows padded to 16 bytes (one extra read and write of that operand).
+ *     If that allocation fails, or the environment variable
+ *     FORGE_MISALIGNED is "loader", an X or dY of the weight-gradient calls
+ *     whose rows are a multiple of 4 bytes is fetched by the kernel itself
+ *     with cp.async instead; other rows need the copy, and a failed
  *     allocation returns FORGE_ERR_CUDA.  forge_wgrad_adamw_noalloc stages
  *     into a fixed buffer instead;
  *   - forge_backward_adamw without a bf16 weight copy (see there).
- * W, m, v, buf are updated in place.  Calls are asynchronous and ordered on `stream`, and can
- * be captured in a CUDA graph once a first call has run on the device; the
- * return value reports only host-side validation
- * and launch errors.  Errors detected on the device (a bounded wait that
+ * W, m, v, buf are updated in place.  Calls are asynchronous and ordered on
+ * `stream`, and can be captured in a CUDA graph once a first call has run
+ * on the device; the return value reports only host-side validation and
+ * launch errors.  Errors detected on the device (a bounded wait that
  * ran out) are recorded in a device status word read by
  * forge_get_device_status().  The library resolves the device addresses of
  * its own device variables (that status word, the no-allocation staging
