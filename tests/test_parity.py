@@ -340,6 +340,27 @@ def test_grouped_many_experts(cuda_device, grouped_form):
     check_grouped(got, X, D, off, W, m, v, 4, sc, False)
 
 
+def test_grouped_rows_outside_every_expert(cuda_device, grouped_form):
+    """offsets[0] > 0 and offsets[E] < T_max: the packed buffer's leading
+    and trailing rows belong to no expert (here non-finite), and no expert's
+    gradient reads them, not even in its first or last partial k-block."""
+    counts = [30, 0, 70, 5]
+    N, M = 264, 392
+    lead, trail = 37, 23
+    X, D, off, W, m, v, sc = grouped_case(counts, N, M, 28)
+    T = int(off[-1])
+    Xb = torch.full((lead + T + trail, N), float("nan"), dtype=torch.bfloat16)
+    Db = torch.full((lead + T + trail, M), float("inf"), dtype=torch.bfloat16)
+    Xb[lead:lead + T] = X[:T]
+    Db[lead:lead + T] = D[:T]
+    offb = np.asarray(off) + lead
+    got = run_grouped(cuda_device, Xb, Db, offb, W, m, v, step=2)
+    assert fg.forge_get_device_status() == fg.FORGE_OK
+    for e in range(len(counts)):
+        assert np.all(np.isfinite(got[0][e])) and np.all(np.isfinite(got[1][e]))
+    check_grouped(got, X, D, off, W, m, v, 2, sc, False)
+
+
 def test_grouped_max_experts(cuda_device, grouped_form):
     """1024 experts, the most one call takes: the expert table fills shared
     memory up to the next carve-out step; ragged counts of 0-5 tokens."""
