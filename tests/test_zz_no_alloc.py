@@ -121,3 +121,24 @@ def test_no_alloc_both_staged_operands_just_under_the_limit(cuda_device, monkeyp
     assert fg.forge_get_device_status() == fg.FORGE_OK
     for a, b in ((W1, W2), (m1, m2), (v1, v2)):
         assert np.array_equal(bits(a), bits(b))
+
+
+def test_no_alloc_loader_mode_still_stages_odd_rows(cuda_device, monkeypatch):
+    """With FORGE_MISALIGNED=loader, X rows of 1044 bytes go to the kernel's
+    cp.async loader, while dY rows of 602 bytes (not a multiple of 4) cannot
+    and are staged into the fixed buffer: both entry points agree bit for
+    bit, call after call."""
+    monkeypatch.setenv("FORGE_MISALIGNED", "loader")
+    dev = cuda_device
+    K, N, M = 300, 522, 301
+    ref = state(N, M, 7, dev)
+    got = tuple(t.clone() for t in ref)
+    for step in (1, 2):
+        X = wl.activations(K, N, wl.seed_of("na-ld-X", step), device=dev)
+        D = wl.activations(K, M, wl.seed_of("na-ld-dY", step), device=dev)
+        fg.forge_wgrad_adamw(X, D, *ref, step=step, **HP)
+        fg.forge_wgrad_adamw_noalloc(X, D, *got, step=step, **HP)
+        torch.cuda.synchronize()
+        assert fg.forge_get_device_status() == fg.FORGE_OK
+        for a, b in zip(ref, got):
+            assert np.array_equal(bits(a), bits(b))
