@@ -65,6 +65,20 @@
  * primary context, so calls after cudaDeviceReset, or from a context other
  * than the primary one, are not supported.
  *
+ * Environment (each read on every call unless noted; none is needed):
+ *   FORGE_MISALIGNED = stage | loader  how X, dY rows TMA cannot address
+ *                      reach the kernel (default stage, see above)
+ *   FORGE_KERNEL = single | pair       the weight-gradient kernel form:
+ *                      one CTA per 128 x 256 tile, or CTA pairs on 256 x 256
+ *                      tiles (default: pairs when d_out > 128)
+ *   FORGE_RASTER_BAND = n              d_out tiles per raster band of the
+ *                      tile walk (default 8; 0 = whole rows); the results
+ *                      do not depend on it
+ *   FORGE_DGRAD_KERNEL = single | pair the dX kernel form (default: pairs
+ *                      unless K fits one 128-token tile)
+ *   FORGE_WAIT_TIMEOUT_MS = ms         limit of every device-side wait
+ *                      (read once per process; default 10000)
+ *
  * Caller preconditions (not checked):
  *   - X and dY do not overlap W, m, v, buf or dW.
  *   - dX = dY W^T has already consumed the old W (the in-place
