@@ -1,0 +1,62 @@
+"""A seeded sweep of random problem shapes against the fp64 oracle: dense
+AdamW and SGD-momentum calls over random K, d_in, d_out (aligned or not,
+bf16 or e4m3 inputs, fp32 or bf16 state) and grouped calls over random
+expert counts.  The shapes are drawn once from a fixed seed, so a failure
+names a reproducible case; sizes stay small enough for the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+from test_parity import (HP, adamw_ref, bf16_inputs, check_adamw, check_grouped, e4m3_inputs,
+                         grouped_case, run_adamw, run_grouped, warm_state)
+
+pytestmark = pytest.mark.gpu
+
+
+def dense_cases(n=48, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        K = int(rng.choice([0, 1, int(rng.integers(2, 700))], p=[0.08, 0.08, 0.84]))
+        N = int(rng.integers(1, 700))
+        M = int(rng.integers(1, 900))
+        kind = "e4m3" if rng.random() < 0.3 else "bf16"
+        state_bf16 = bool(rng.random() < 0.4)
+        out.append((i, K, N, M, kind, state_bf16))
+    return out
+
+
+def grouped_cases(n=16, seed=2025):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        E = int(rng.integers(1, 12))
+        counts = rng.integers(0, 160, size=E)
+        counts[rng.random(E) < 0.3] = 0
+        N = int(rng.integers(8, 520))
+        M = int(rng.integers(8, 600))
+        kind = "e4m3" if rng.random() < 0.3 else "bf16"
+        out.append((i, [int(c) for c in counts], N, M, kind))
+    return out
+
+
+@pytest.mark.parametrize("i,K,N,M,kind,state_bf16", dense_cases(),
+                         ids=lambda v: str(v) if not isinstance(v, bool) else ("bf16st" if v else "f32st"))
+def test_random_dense_adamw(cuda_device, i, K, N, M, kind, state_bf16):
+    if kind == "bf16":
+        X, D = bf16_inputs(K, N, M, 300 + i)
+        sc = None
+    else:
+        X, D, sc = e4m3_inputs(K, N, M, 300 + i)
+    W, m, v = warm_state(N, M, 400 + i, state_bf16)
+    got = run_adamw(cuda_device, X, D, W, m, v, step=3, scales=sc)
+    G = oracle.wgrad(X, D, scales=sc or (1.0, 1.0))
+    ref = adamw_ref(G, W, m, v, step=3, **vars(HP))
+    check_adamw(got, ref, G, HP.lr, state_bf16)
+
+
+@pytest.mark.parametrize("i,counts,N,M,kind", grouped_cases(), ids=lambda v: str(v)[:24])
+def test_random_grouped_adamw(cuda_device, i, counts, N, M, kind):
+    X, D, off, W, m, v, sc = grouped_case(counts, N, M, 500 + i, kind=kind)
+    got = run_grouped(cuda_device, X, D, off, W, m, v, step=2, scales=sc)
+    check_grouped(got, X, D, off, W, m, v, 2, sc, False)
