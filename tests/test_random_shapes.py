@@ -60,3 +60,32 @@ def test_random_grouped_adamw(cuda_device, i, counts, N, M, kind):
     X, D, off, W, m, v, sc = grouped_case(counts, N, M, 500 + i, kind=kind)
     got = run_grouped(cuda_device, X, D, off, W, m, v, step=2, scales=sc)
     check_grouped(got, X, D, off, W, m, v, 2, sc, False)
+
+
+@pytest.mark.parametrize("i,K,N,M,kind,state_bf16", dense_cases(n=8, seed=2026),
+                         ids=lambda v: str(v) if not isinstance(v, bool) else ("bf16st" if v else "f32st"))
+def test_random_dense_sgdm(cuda_device, i, K, N, M, kind, state_bf16):
+    import torch
+
+    import weight_grad_gemm_gb300 as fg
+    from parity_util import check_state_bf16, check_state_f32, rms
+    from test_parity import dev_state, host_state, scales_dev
+    if kind == "bf16":
+        X, D = bf16_inputs(K, N, M, 600 + i)
+        sc = None
+    else:
+        X, D, sc = e4m3_inputs(K, N, M, 600 + i)
+    W, buf, _ = warm_state(N, M, 700 + i, state_bf16)
+    lr, mu, wd = float(np.float32(1e-2)), float(np.float32(0.9)), float(np.float32(0.05))
+    Wd, bd = dev_state(W, cuda_device), dev_state(buf, cuda_device)
+    fg.forge_wgrad_sgdm(X.to(cuda_device), D.to(cuda_device), Wd, bd, lr=lr, momentum=mu, wd=wd,
+                        scales=None if sc is None else scales_dev(sc, cuda_device))
+    torch.cuda.synchronize()
+    G = oracle.wgrad(X, D, scales=sc or (1.0, 1.0))
+    ref = oracle.sgdm(G, W, buf, lr=lr, momentum=mu, wd=wd)
+    if state_bf16:
+        check_state_bf16(host_state(bd), ref["buf_exact"], "buf")
+    else:
+        check_state_f32(host_state(bd), ref["buf_exact"], "buf")
+    err = np.max(np.abs(host_state(Wd).astype(np.float64) - ref["W_exact"]))
+    assert err <= 2e-3 * lr * rms(ref["buf_exact"]) + 2 * np.finfo(np.float32).eps * 0.1
