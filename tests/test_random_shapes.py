@@ -1,7 +1,8 @@
 """A seeded sweep of random problem shapes against the fp64 oracle: dense
 AdamW and SGD-momentum calls over random K, d_in, d_out (aligned or not,
-bf16 or e4m3 inputs, fp32 or bf16 state) and grouped calls over random
-expert counts.  The shapes are drawn once from a fixed seed, so a failure
+bf16 or e4m3 inputs, fp32 or bf16 state), grouped calls over random expert
+counts, multi-problem calls over random problem counts and widths, and
+dX = dY Wb^T over random shapes.  The shapes are drawn once from a fixed seed, so a failure
 names a reproducible case; sizes stay small enough for the oracle."""
 import numpy as np
 import pytest
@@ -89,3 +90,44 @@ def test_random_dense_sgdm(cuda_device, i, K, N, M, kind, state_bf16):
         check_state_f32(host_state(bd), ref["buf_exact"], "buf")
     err = np.max(np.abs(host_state(Wd).astype(np.float64) - ref["W_exact"]))
     assert err <= 2e-3 * lr * rms(ref["buf_exact"]) + 2 * np.finfo(np.float32).eps * 0.1
+
+
+def multi_cases(n=6, seed=2027):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        P = int(rng.integers(1, 9))
+        Ms = [int(rng.integers(1, 700)) for _ in range(P)]
+        K = int(rng.integers(0, 400))
+        N = int(rng.integers(1, 600))
+        out.append((i, K, N, Ms, bool(rng.random() < 0.5)))
+    return out
+
+
+@pytest.mark.parametrize("i,K,N,Ms,state_bf16", multi_cases(), ids=lambda v: str(v)[:30])
+def test_random_multi(cuda_device, i, K, N, Ms, state_bf16):
+    from test_multi import case, run_multi
+    X, Ds, states = case(K, N, Ms, 800 + i, state_bf16)
+    got = run_multi(cuda_device, X, Ds, states, step=2)
+    for D, (W, m, v), g in zip(Ds, states, got):
+        G = oracle.wgrad(X, D)
+        check_adamw(g, adamw_ref(G, W, m, v, step=2, **vars(HP)), G, HP.lr, state_bf16)
+
+
+def dgrad_cases(n=8, seed=2028):
+    rng = np.random.default_rng(seed)
+    return [(i, int(rng.integers(1, 600)), int(rng.integers(1, 600)), int(rng.integers(1, 900)))
+            for i in range(n)]
+
+
+@pytest.mark.parametrize("i,K,N,M", dgrad_cases(), ids=lambda v: str(v))
+def test_random_dgrad(cuda_device, i, K, N, M):
+    import torch
+
+    import weight_grad_gemm_gb300 as fg
+    from test_dgrad import check_dx, inputs
+    D, Wb = inputs(K, N, M, 900 + i, cuda_device)
+    dX = torch.full((K, N), float("nan"), dtype=torch.bfloat16, device=cuda_device)
+    fg.forge_dgrad(D, Wb, dX)
+    torch.cuda.synchronize()
+    check_dx(dX, oracle.dgrad(oracle.as_bits(D.cpu()), oracle.as_bits(Wb.cpu())))
