@@ -16,6 +16,7 @@ The step on rank r:
     2. reduce-scatter: rank r receives the sum of rows     torch.distributed
        ranges[r] over all ranks                            (NCCL on GPUs)
     3. AdamW (or SGD-momentum) on its shard of W, m, v     forge_owner_adamw
+                                                           (forge_owner_sgdm)
 This path materialises the partial gradients (the collective exchanges
 them), so the zero-grad_W-bytes property of the fused single-GPU calls does
 not apply to it.
@@ -99,3 +100,22 @@ def owner_adamw_step(X, dY, W_shard, m_shard, v_shard, ranges, *, lr, beta1, bet
     if r1 > r0:
         fg.forge_owner_adamw(shard, W_shard, m_shard, v_shard, lr=lr, beta1=beta1, beta2=beta2,
                              eps=eps, wd=wd, step=step)
+
+
+def owner_sgdm_step(X, dY, W_shard, mom_shard, ranges, *, lr, momentum, wd, scales=None,
+                    grad=None, group=None):
+    """owner_adamw_step with SGD-momentum: the partial dW of this rank's
+    tokens, the reduce-scatter, and the owner's SGD-momentum step on its
+    rows of W and the momentum buffer."""
+    import torch
+    import torch.distributed as dist
+
+    import weight_grad_gemm_gb300 as fg
+    N, M = X.shape[1], dY.shape[1]
+    if grad is None:
+        grad = torch.empty((N, M), dtype=torch.float32, device=X.device)
+    fg.forge_wgrad_only(X, dY, grad, scales=scales)
+    shard = reduce_scatter_rows(grad, ranges, group)
+    r0, r1 = ranges[dist.get_rank(group)]
+    if r1 > r0:
+        fg.forge_owner_sgdm(shard, W_shard, mom_shard, lr=lr, momentum=momentum, wd=wd)
