@@ -260,3 +260,41 @@ def test_owner_step_full_size_mlp_shapes_bitwise(cuda_device):
     assert fg.forge_get_device_status() == fg.FORGE_OK
     for a, b in zip(fused, own):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("opt", ["adamw", "sgdm"])
+def test_owner_step_through_nccl_one_rank(cuda_device, opt):
+    """The user-facing step (partial dW, NCCL reduce-scatter, owner update)
+    on a one-rank NCCL group: the collective is then a copy, and the step
+    must equal the fused call bit for bit."""
+    import torch
+    import torch.distributed as dist
+
+    import weight_grad_gemm_gb300 as fg
+    from test_parity import bf16_inputs, dev_state, warm_state
+    dev = cuda_device
+    K, N, M = 200, 520, 392
+    X, D = bf16_inputs(K, N, M, 66)
+    W, m, v = warm_state(N, M, 67)
+    Xd, Dd = X.to(dev), D.to(dev)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(free_port()))
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=dev)
+    try:
+        ranges = owner.owner_ranges(N, 1)
+        fused = [dev_state(a, dev) for a in (W, m, v)]
+        own = [dev_state(a, dev) for a in (W, m, v)]
+        if opt == "adamw":
+            hp = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.01)
+            fg.forge_wgrad_adamw(Xd, Dd, *fused, step=2, **hp)
+            owner.owner_adamw_step(Xd, Dd, *own, ranges, step=2, **hp)
+        else:
+            hp = dict(lr=1e-2, momentum=0.9, wd=0.05)
+            fg.forge_wgrad_sgdm(Xd, Dd, fused[0], fused[1], **hp)
+            owner.owner_sgdm_step(Xd, Dd, own[0], own[1], ranges, **hp)
+        torch.cuda.synchronize()
+    finally:
+        dist.destroy_process_group()
+    n = 3 if opt == "adamw" else 2
+    for a, b in zip(fused[:n], own[:n]):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
