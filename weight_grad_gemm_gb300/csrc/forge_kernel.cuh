@@ -1119,10 +1119,8 @@ constexpr int kPairStageBytes = kPairStageA + kPairStageB;
 #endif
 // Operand stages per CTA: dense and multi-problem calls six (the 196 KB
 // carve-out step, a 60 KB L1); grouped calls FORGE_GROUPED_PAIR_STAGES
-// (compile time, default six).  The ring and L1 share the SM's 256 KB: the
-// ring covers the operand loads' latency, L1 holds the epilogue's state
-// loads in flight.  On the MoE layer five stages (the 164 KB step, a 92 KB
-// L1) measured 3% slower and seven (the 228 KB step, a 28 KB L1) 5-7%.
+// (compile time).  The ring and L1 share the SM's 256 KB: the ring covers the
+// operand loads' latency, L1 holds the epilogue's state loads in flight.
 template <bool GROUPED>
 struct PairRing {
     static constexpr int stages = GROUPED ? FORGE_GROUPED_PAIR_STAGES : 6;
